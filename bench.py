@@ -1,0 +1,400 @@
+"""Benchmark of the FP32 SGEMM path on GB300: prints ONE JSON line.
+
+A step is one sgemm_f32 call, C = alpha * A * B + beta * C, on the 8192^3 workload
+(A, B uniform[-1, 1), C N(0, 1), seed 3, alpha = 0.5, beta = 2). Inputs (805 MB) are larger
+than the 129 MB L2, so no flush is needed between steps. C is updated in place each step;
+with beta = 2 its magnitude doubles per step, which stays far from overflow for the step
+counts used here and does not change the work.
+
+value   = 2 M N K x steps x ranks / (max over ranks of the CUDA-event time of the steps)
+e2e     = the same metric with each step's A, B, C copied from pinned host memory to the
+          device and C copied back, inside the timed region
+roofline: FP32 FFMA pipe ("alu"): SMs x 128 lanes x 2 FLOP x max SM clock
+cpu_baseline: the CPU FP64 oracle on a bounded sample of rows of the same workload.
+
+`--impl reference` times that oracle instead (the only reference this study has: the
+pages ship no library), on the same workload and metric.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one independent replica per GPU (the problem does not shard).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import BY_NAME, HEADLINE, workload_inputs  # noqa: E402
+
+METRIC = "SGEMM TFLOPS (2MNK/t) at 4096³ and 8192³; fraction of GB300 FP32 peak"
+UNIT = "TFLOP/s"
+FP32_LANES_PER_SM = 128  # Blackwell SM: 4 partitions x 32 FP32 lanes
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=HEADLINE.name)
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------------------------
+# distributed plumbing (replicas only: barrier and max-over-ranks timing)
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------------------------
+# clock sampling during the timed region
+
+REASON_COLS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+class ClockSampler:
+    def __init__(self, bus_id: str | None):
+        self.bus_id = bus_id
+        self.proc = None
+        self.lines: list[str] = []
+        self.th = None
+
+    def start(self):
+        q = ("pci.bus_id,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.th = threading.Thread(target=self._read, daemon=True)
+        self.th.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict | None:
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.th:
+            self.th.join(timeout=2)
+        rows = []
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            if self.bus_id and self.bus_id.lower() not in f[0].lower():
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), float(f[3]), f[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        power = [r[2] for r in rows]
+        loaded = [r for r in rows if r[2] >= 0.5 * max(power)] or rows
+        reasons = sorted({REASON_COLS[i] for r in loaded for i, v in enumerate(r[3])
+                          if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in loaded),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons,
+                "samples": len(loaded), "power_w_max": max(power)}
+
+
+def bus_id_of(dev: int) -> str | None:
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_bus_id:02X}:{p.pci_device_id:02X}."
+    except Exception:
+        return None
+
+
+def max_sm_clock_mhz() -> float:
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=clocks.max.sm",
+                              "--format=csv,noheader,nounits"], capture_output=True,
+                             text=True, timeout=30).stdout.split()
+        return float(out[0])
+    except Exception:
+        return 2070.0  # GB300 maximum SM clock
+
+
+# ------------------------------------------------------------------------------------
+# CPU oracle leg
+
+def cpu_oracle_sample(w, A, B, C, seconds: float, rows_hint: int | None = None):
+    """Time the oracle on a bounded set of rows; returns (TFLOP/s, rows, seconds, R, S)."""
+    import oracle
+    rng = np.random.default_rng(12345)
+    probe = np.sort(rng.choice(w.M, size=min(w.M, 4), replace=False))
+    t0 = time.perf_counter()
+    oracle.sgemm_f64_rows(A, B, C, w.alpha, w.beta, probe)
+    dt = max(time.perf_counter() - t0, 1e-6)
+    nrows = rows_hint or int(max(1, min(w.M, seconds / (dt / len(probe)))))
+    rows = np.sort(rng.choice(w.M, size=nrows, replace=False))
+    t0 = time.perf_counter()
+    R, S = oracle.sgemm_f64_rows(A, B, C, w.alpha, w.beta, rows)
+    t = time.perf_counter() - t0
+    return 2.0 * nrows * w.N * w.K / t / 1e12, rows, t, R, S, oracle.threads()
+
+
+def reference_arm(args, dist: Dist):
+    """`--impl reference`: the CPU FP64 oracle timed on the host cores."""
+    if dist.rank != 0:
+        return
+    w = BY_NAME[args.workload]
+    A, B, C = workload_inputs(w)
+    per_step = max(1.0, min(6.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, rows, _, _, _, cores = cpu_oracle_sample(w, A, B, C, per_step)
+    import oracle
+    for _ in range(args.warmup):
+        oracle.sgemm_f64_rows(A, B, C, w.alpha, w.beta, rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.sgemm_f64_rows(A, B, C, w.alpha, w.beta, rows)
+    t = time.perf_counter() - t0
+    value = 2.0 * len(rows) * w.N * w.K * args.steps / t / 1e12
+    sample = (f"{len(rows)} of {w.M} output rows (all {w.N} columns, full K={w.K}) per "
+              f"step, FP64 accumulation")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(w):
+    return {"workload": f"sgemm {w.M}x{w.N}x{w.K} fp32 row-major packed, A,B "
+                        f"{w.ab_dist} C {w.c_dist} seed {w.seed}, alpha={w.alpha} "
+                        f"beta={w.beta}",
+            "M": w.M, "N": w.N, "K": w.K, "alpha": w.alpha, "beta": w.beta,
+            "parallelism": "replicas (one independent problem per GPU)",
+            "l2": "inputs larger than L2 (no flush needed)"}
+
+
+# ------------------------------------------------------------------------------------
+
+def time_steps(fn, steps, stream):
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    end.synchronize()
+    return start.elapsed_time(end) / 1e3
+
+
+def our_arm(args, dist: Dist):
+    import dense_fp32_matrix_08_gb300 as sg
+
+    dev = dist.local if dist.world > 1 else 0
+    torch.cuda.set_device(dev)
+    w = BY_NAME[args.workload]
+    M, N, K = w.M, w.N, w.K
+    A, B, C0 = workload_inputs(w)
+    stream = torch.cuda.Stream()
+    s_handle = stream.cuda_stream
+    dA, dB, dC = A.cuda(), B.cuda(), C0.cuda()
+    torch.cuda.synchronize()
+
+    plan = sg.sgemm_f32_plan(M, N, K, K, N, N, w.alpha, w.beta, 0)
+    assert plan["status"] == 0, plan
+
+    def step():
+        rc = sg.lib.sgemm_f32(M, N, K, w.alpha, dA.data_ptr(), K, dB.data_ptr(), N, w.beta,
+                              dC.data_ptr(), N, s_handle)
+        if rc != 0:
+            raise RuntimeError(f"sgemm_f32 returned {rc}")
+
+    # first call on the pristine C: kept for the oracle check in the CPU-baseline leg
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    first_rows = None
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        tf, rows, t, R, S, cores = cpu_oracle_sample(w, A, B, C0, args.cpu_seconds)
+        got = dC[torch.as_tensor(rows, device="cuda")].cpu().numpy().astype(np.float64)
+        tol = 1e-4 * (S + np.abs(np.float32(w.beta) * C0.numpy()[rows].astype(np.float64)))
+        err = np.abs(got - R)
+        cpu = {"value": tf, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{len(rows)} random output rows of {M} (all {N} columns, full "
+                         f"K={K}), FP64, {t:.1f} s",
+               "parity": {"rows": len(rows), "max_err_over_tol": float(np.max(err / tol)),
+                          "ok": bool(np.all(err <= tol))}}
+    del first_rows
+
+    for _ in range(args.warmup):
+        with torch.cuda.stream(stream):
+            step()
+    stream.synchronize()
+
+    sampler = ClockSampler(bus_id_of(dev))
+    sampler.start()
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        elapsed = time_steps(step, args.steps, stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    t_max = dist.max(elapsed)
+    flops = 2.0 * M * N * K
+    value = flops * args.steps * dist.world / t_max / 1e12
+    ms = 1e3 * t_max / args.steps
+
+    # dominant kernel: with a single-launch plan the step time is the kernel's duration
+    props = torch.cuda.get_device_properties(dev)
+    max_mhz = (clocks or {}).get("sm_max_mhz") or max_sm_clock_mhz()
+    peak = props.multi_processor_count * FP32_LANES_PER_SM * 2 * max_mhz * 1e6 / 1e12
+    achieved = flops * args.steps / elapsed / 1e12
+    roof = {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "traffic": None,
+            "peak_basis": f"{props.multi_processor_count} SMs x {FP32_LANES_PER_SM} FP32 "
+                          f"lanes x 2 FLOP x {max_mhz:.0f} MHz (max SM clock)",
+            "kernel_launches_per_step": plan["launches"]}
+    if clocks and clocks.get("sm_mhz"):
+        roof["frac_at_sampled_clock"] = achieved / (peak * clocks["sm_mhz"] / max_mhz)
+
+    # end to end: host buffers in pinned memory, copies inside the timed region
+    hA, hB, hC = A.pin_memory(), B.pin_memory(), C0.pin_memory()
+    hOut = torch.empty_like(hC).pin_memory()
+
+    def e2e_step():
+        dA.copy_(hA, non_blocking=True)
+        dB.copy_(hB, non_blocking=True)
+        dC.copy_(hC, non_blocking=True)
+        step()
+        hOut.copy_(dC, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+        stream.synchronize()
+        dist.barrier()
+        e2e_t = time_steps(e2e_step, args.e2e_steps, stream)
+    e2e_t = dist.max(e2e_t)
+    e2e = {"value": flops * args.e2e_steps * dist.world / e2e_t / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": 4 * (M * K + K * N + M * N), "d2h_bytes_per_step": 4 * M * N,
+           "ms_per_step": 1e3 * e2e_t / args.e2e_steps}
+
+    secondary = {}
+    if not args.no_secondary and w.name == HEADLINE.name:
+        w2 = BY_NAME["sgemm_4096cube"]
+        A2, B2, C2 = (x.cuda() for x in workload_inputs(w2))
+        p2 = sg.sgemm_f32_plan(w2.M, w2.N, w2.K, w2.K, w2.N, w2.N, w2.alpha, w2.beta, 0)
+
+        def step2():
+            rc = sg.lib.sgemm_f32(w2.M, w2.N, w2.K, w2.alpha, A2.data_ptr(), w2.K,
+                                  B2.data_ptr(), w2.N, w2.beta, C2.data_ptr(), w2.N,
+                                  s_handle)
+            if rc != 0:
+                raise RuntimeError(f"sgemm_f32 returned {rc}")
+
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                step2()
+            t2 = time_steps(step2, args.steps, stream)
+        secondary[w2.name] = {"value": w2.flops * args.steps / t2 / 1e12, "unit": UNIT,
+                              "ms_per_step": 1e3 * t2 / args.steps,
+                              "frac": w2.flops * args.steps / t2 / 1e12 / peak,
+                              "launches_per_step": p2["launches"],
+                              "l2": "inputs 201 MB > L2 (no flush)"}
+
+    if dist.rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic", "config": _config(w),
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": plan["launches"] * args.steps,
+            "plan": {k: plan[k] for k in ("variant", "split", "launches", "ws_bytes")},
+            "impl": "ours",
+        }
+        if secondary:
+            line["secondary"] = secondary
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            reference_arm(args, dist)
+        else:
+            our_arm(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+"""Python binding of the sgemm_f32 C ABI (include/sgemm_f32.h).
+
+Argument marshalling only: every step of C = alpha * A * B + beta * C runs in the CUDA
+kernels of libsgemm_f32.so. Loading fails loudly if the library has not been built; there
+is no fallback implementation.
+
+Pointer arguments accept either integers (device addresses) or torch CUDA tensors (their
+data_ptr() is passed; the tensor must be float32). `stream` accepts an integer handle, a
+torch.cuda.Stream, or None for torch's current stream on the current device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as LIB_PATH
+
+__all__ = [
+    "LIB_PATH", "SgemmError", "lib", "sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced",
+    "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
+    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm", "EXPORTED",
+]
+
+# Every symbol include/sgemm_f32.h declares.
+EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspace_size",
+            "sgemm_f32_plan", "sgemm_f32_num_variants", "sgemm_f32_variant_info",
+            "sgemm_f32_version")
+
+
+class SgemmError(RuntimeError):
+    """A nonzero status from the library: negative = illegal argument index, positive =
+    cudaError_t."""
+
+    def __init__(self, status: int, what: str = "sgemm_f32"):
+        self.status = status
+        super().__init__(f"{what} returned {status}")
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build the CUDA library first "
+            "(python -c 'import __graft_entry__ as g; g.build()')")
+    L = ctypes.CDLL(LIB_PATH)
+    i, f, vp, sz = ctypes.c_int, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+    pi, psz = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)
+    gemm = [i, i, i, f, vp, i, vp, i, f, vp, i]
+    L.sgemm_f32.argtypes = gemm + [vp]
+    L.sgemm_f32_ws.argtypes = gemm + [vp, sz, vp]
+    L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
+    L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
+    L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, psz]
+    L.sgemm_f32_num_variants.argtypes = []
+    L.sgemm_f32_variant_info.argtypes = [i] + [pi] * 7
+    L.sgemm_f32_version.argtypes = []
+    L.sgemm_f32_version.restype = ctypes.c_char_p
+    for name in EXPORTED:
+        if name != "sgemm_f32_version":
+            getattr(L, name).restype = ctypes.c_int
+    return L
+
+
+lib = _load()
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    import torch
+    if isinstance(x, torch.Tensor):
+        if x.dtype != torch.float32:
+            raise TypeError("tensor operands must be float32")
+        if x.numel() and not x.is_cuda:
+            raise TypeError("tensor operands must live on a CUDA device")
+        return x.data_ptr() or None
+    raise TypeError(f"cannot pass {type(x).__name__} as a device pointer")
+
+
+def _stream(s) -> int | None:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, int):
+        return s or None
+    return int(s.cuda_stream) or None
+
+
+def sgemm_f32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """Mirror of the C entry point; returns its status (0 = success)."""
+    return lib.sgemm_f32(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                         _stream(stream))
+
+
+def sgemm_f32_ws(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, workspace, workspace_bytes,
+                 stream=None) -> int:
+    return lib.sgemm_f32_ws(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+                            _ptr(workspace), workspace_bytes, _stream(stream))
+
+
+def sgemm_f32_forced(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant, split,
+                     stream=None) -> int:
+    return lib.sgemm_f32_forced(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
+                                ldc, variant, split, _stream(stream))
+
+
+def sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc) -> tuple[int, int]:
+    """(status, bytes)."""
+    b = ctypes.c_size_t(0)
+    rc = lib.sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc, ctypes.byref(b))
+    return rc, b.value
+
+
+def sgemm_f32_plan(M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0, num_sms=0) -> dict:
+    v, s, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    rc = lib.sgemm_f32_plan(M, N, K, lda, ldb, ldc, alpha, beta, num_sms, ctypes.byref(v),
+                            ctypes.byref(s), ctypes.byref(n), ctypes.byref(ws))
+    return {"status": rc, "variant": v.value, "split": s.value, "launches": n.value,
+            "ws_bytes": ws.value}
+
+
+def sgemm_f32_num_variants() -> int:
+    return lib.sgemm_f32_num_variants()
+
+
+def sgemm_f32_variant_info(v: int) -> dict | None:
+    vals = [ctypes.c_int(0) for _ in range(7)]
+    if lib.sgemm_f32_variant_info(v, *[ctypes.byref(x) for x in vals]) != 0:
+        return None
+    keys = ("BM", "BN", "BK", "threads", "TM", "TN", "stages")
+    return dict(zip(keys, (x.value for x in vals)))
+
+
+def sgemm_f32_version() -> str:
+    return lib.sgemm_f32_version().decode()
+
+
+def sgemm(A, B, C, alpha: float = 1.0, beta: float = 0.0, stream=None):
+    """C = alpha * A @ B + beta * C in place on 2-D float32 CUDA tensors (row-major views
+    with unit column stride; the row stride is passed as the leading dimension). Raises
+    SgemmError on a nonzero status. Returns C."""
+    for name, t in (("A", A), ("B", B), ("C", C)):
+        if t.dim() != 2:
+            raise ValueError(f"{name} must be 2-D")
+        if t.size(1) > 1 and t.stride(1) != 1:
+            raise ValueError(f"{name} must have unit column stride")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K or tuple(C.shape) != (M, N):
+        raise ValueError("shape mismatch")
+
+    def ld(t):
+        return max(t.stride(0) if t.size(0) > 1 else t.size(1), 1)
+
+    rc = sgemm_f32(M, N, K, alpha, A, ld(A), B, ld(B), beta, C, ld(C), stream)
+    if rc != 0:
+        raise SgemmError(rc)
+    return C

@@ -1,0 +1,259 @@
+// C ABI of the FP32 SGEMM library: argument checks, launch planning and dispatch.
+// The operation and its contract are documented in include/sgemm_f32.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/sgemm_f32.h"
+#include "sgemm_aux.cuh"
+#include "sgemm_ffma.cuh"
+#include "sgemm_plan.h"
+
+namespace sgemm {
+
+// ------------------------------------------------------------------------------------
+// Tile configurations. Their shapes are also listed, without CUDA, in sgemm_plan.h
+// (kVariants); a static_assert below keeps the two in step.
+using V0 = TileConfig<128, 256, 16, 64, 64, 16, 8, 3, 1>;  // large tiles, 128 acc/thread
+using V1 = TileConfig<128, 128, 16, 32, 64, 8, 8, 4, 2>;   // 8x8 per thread, 2 CTAs/SM
+using V2 = TileConfig<64, 64, 16, 32, 32, 8, 4, 4, 4>;     // small tiles for small problems
+using V3 = TileConfig<16, 256, 32, 16, 64, 8, 4, 3, 2>;    // thin M (M <= 16 per tile)
+using V4 = TileConfig<256, 16, 32, 64, 16, 8, 4, 3, 2>;    // thin N (N <= 16 per tile)
+
+template <class Cfg>
+constexpr bool matches(const VariantShape &s) {
+  return s.BM == Cfg::BM && s.BN == Cfg::BN && s.BK == Cfg::BK && s.threads == Cfg::NT &&
+         s.TM == Cfg::TM && s.TN == Cfg::TN && s.stages == Cfg::STAGES &&
+         s.min_blocks == Cfg::MIN_BLOCKS && s.smem_bytes == Cfg::SMEM_BYTES;
+}
+static_assert(kNumVariants == 5, "variant table size");
+static_assert(matches<V0>(kVariants[0]) && matches<V1>(kVariants[1]) &&
+                  matches<V2>(kVariants[2]) && matches<V3>(kVariants[3]) &&
+                  matches<V4>(kVariants[4]),
+              "sgemm_plan.h variant table out of step with the kernel configurations");
+
+using KernelFn = void (*)(const GemmParams);
+
+struct VariantKernels {
+  KernelFn k[2][2];  // [vec_b][split]
+  int threads;
+  int smem;
+};
+
+template <class Cfg>
+constexpr VariantKernels make_kernels() {
+  return VariantKernels{{{sgemm_ffma_kernel<Cfg, false, false>, sgemm_ffma_kernel<Cfg, false, true>},
+                         {sgemm_ffma_kernel<Cfg, true, false>, sgemm_ffma_kernel<Cfg, true, true>}},
+                        Cfg::NT,
+                        Cfg::SMEM_BYTES};
+}
+
+static const VariantKernels kKernels[kNumVariants] = {
+    make_kernels<V0>(), make_kernels<V1>(), make_kernels<V2>(), make_kernels<V3>(),
+    make_kernels<V4>()};
+
+// ------------------------------------------------------------------------------------
+// Per-device one-time setup: opt every kernel into its dynamic shared memory and cache
+// the SM count.
+constexpr int kMaxDevices = 64;
+struct DeviceState {
+  std::once_flag once;
+  int num_sms = 0;
+  cudaError_t err = cudaSuccess;
+};
+static DeviceState g_dev[kMaxDevices];
+
+static cudaError_t device_setup(int *num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  DeviceState &st = g_dev[dev];
+  std::call_once(st.once, [&st, dev]() {
+    int sms = 0;
+    cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    for (int v = 0; v < kNumVariants && err == cudaSuccess; ++v)
+      for (int a = 0; a < 2 && err == cudaSuccess; ++a)
+        for (int b = 0; b < 2 && err == cudaSuccess; ++b)
+          err = cudaFuncSetAttribute(kKernels[v].k[a][b],
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kKernels[v].smem);
+    st.num_sms = sms;
+    st.err = err;
+  });
+  *num_sms = st.num_sms;
+  return st.err;
+}
+
+static inline bool aligned16(const void *p) {
+  return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+static int grid_for_stream_kernel(long long work_items, int num_sms) {
+  const long long blocks = (work_items + 255) / 256;
+  const long long cap = (long long)num_sms * 8;
+  return (int)std::max<long long>(1, std::min(blocks, cap));
+}
+
+// Enqueue the whole computation for a validated, non-empty problem.
+static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
+               const float *B, float beta, float *C, float *ws, int num_sms,
+               cudaStream_t stream) {
+  const bool vec_c = (pr.ldc % 4 == 0) && aligned16(C);
+  if (pl.variant < 0) {  // alpha == 0 or K == 0: C = beta * C
+    if (beta == 1.0f) return 0;
+    const long long work = (long long)pr.M * ((pr.N + 3) / 4);
+    scale_c_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+        C, pr.ldc, pr.M, pr.N, beta, vec_c ? 1 : 0);
+    return (int)cudaGetLastError();
+  }
+  const VariantShape &vs = kVariants[pl.variant];
+  GemmParams p;
+  p.M = pr.M;
+  p.N = pr.N;
+  p.K = pr.K;
+  p.alpha = alpha;
+  p.beta = beta;
+  p.A = A;
+  p.lda = pr.lda;
+  p.B = B;
+  p.ldb = pr.ldb;
+  p.C = C;
+  p.ldc = pr.ldc;
+  p.ws = ws;
+  p.ldw = workspace_ld(pr.N);
+  p.k_per_split = pl.k_per_split;
+  p.tiles_m = pl.tiles_m;
+  p.tiles_n = pl.tiles_n;
+  p.group_m = pl.group_m;
+  p.vec_c = vec_c ? 1 : 0;
+  const bool vec_b = (pr.ldb % 4 == 0) && aligned16(B);
+  const bool split = pl.split > 1;
+  if ((long long)pl.tiles_m * pl.tiles_n > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
+  dim3 grid((unsigned)(pl.tiles_m * pl.tiles_n), (unsigned)pl.split, 1);
+  kKernels[pl.variant].k[vec_b][split]<<<grid, vs.threads, vs.smem_bytes, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return (int)e;
+  if (split) {
+    const long long work = (long long)pr.M * ((pr.N + 3) / 4);
+    splitk_reduce_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+        ws, p.ldw, pl.split, pr.M, pr.N, alpha, beta, C, pr.ldc, vec_c ? 1 : 0);
+    e = cudaGetLastError();
+  }
+  return (int)e;
+}
+
+// Shared body of the computing entry points. ws_mode: 0 = allocate on the stream,
+// 1 = caller workspace (ws, ws_bytes).
+static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda,
+                       const float *B, int ldb, float beta, float *C, int ldc, int force_v,
+                       int force_split, int ws_mode, void *ws, size_t ws_bytes,
+                       cudaStream_t stream) {
+  Problem pr{M, N, K, lda, ldb, ldc};
+  int rc = validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
+  if (rc != 0) return rc;
+  if (M == 0 || N == 0) return 0;
+  if (force_v >= kNumVariants || force_v < -1) return kErrBadVariant;
+  int num_sms = 0;
+  cudaError_t e = device_setup(&num_sms);
+  if (e != cudaSuccess) return (int)e;
+  Plan pl = make_plan(pr, alpha, beta, num_sms, force_v, force_split);
+  float *wsp = nullptr;
+  if (pl.ws_bytes > 0) {
+    if (ws_mode == 1) {
+      if (ws == nullptr || ws_bytes < pl.ws_bytes || !aligned16(ws)) return kErrWorkspace;
+      wsp = static_cast<float *>(ws);
+    } else {
+      e = cudaMallocAsync(reinterpret_cast<void **>(&wsp), pl.ws_bytes, stream);
+      if (e != cudaSuccess) return (int)e;
+    }
+  }
+  rc = run(pr, pl, alpha, A, B, beta, C, wsp, num_sms, stream);
+  if (ws_mode == 0 && wsp != nullptr) {
+    e = cudaFreeAsync(wsp, stream);
+    if (rc == 0 && e != cudaSuccess) rc = (int)e;
+  }
+  return rc;
+}
+
+}  // namespace sgemm
+
+using namespace sgemm;
+
+extern "C" {
+
+int sgemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+              int ldb, float beta, float *C, int ldc, cudaStream_t stream) {
+  return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, -1, 0, 0, nullptr, 0,
+                     stream);
+}
+
+int sgemm_f32_ws(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                 int ldb, float beta, float *C, int ldc, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+  return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, -1, 0, 1, workspace,
+                     workspace_bytes, stream);
+}
+
+int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
+                     const float *B, int ldb, float beta, float *C, int ldc, int variant,
+                     int split, cudaStream_t stream) {
+  return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant, split, 0,
+                     nullptr, 0, stream);
+}
+
+int sgemm_f32_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
+                             size_t *bytes) {
+  return sgemm_f32_plan(M, N, K, lda, ldb, ldc, 1.0f, 1.0f, 0, nullptr, nullptr, nullptr,
+                        bytes);
+}
+
+int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta,
+                   int num_sms, int *variant, int *split, int *launches, size_t *ws_bytes) {
+  Problem pr{M, N, K, lda, ldb, ldc};
+  int rc = validate(pr, alpha, true, true, true);
+  if (rc != 0) return rc;
+  if (num_sms <= 0) {
+    cudaError_t e = device_setup(&num_sms);
+    if (e != cudaSuccess) return (int)e;
+  }
+  Plan pl;
+  if (M == 0 || N == 0) {
+    pl.variant = -1;
+    pl.split = 1;
+    pl.launches = 0;
+    pl.ws_bytes = 0;
+  } else {
+    pl = make_plan(pr, alpha, beta, num_sms, -1, 0);
+  }
+  if (variant) *variant = pl.variant;
+  if (split) *split = pl.split;
+  if (launches) *launches = pl.launches;
+  if (ws_bytes) *ws_bytes = pl.ws_bytes;
+  return 0;
+}
+
+int sgemm_f32_num_variants(void) { return kNumVariants; }
+
+int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *TM, int *TN,
+                           int *stages) {
+  if (v < 0 || v >= kNumVariants) return -1;
+  const VariantShape &s = kVariants[v];
+  if (BM) *BM = s.BM;
+  if (BN) *BN = s.BN;
+  if (BK) *BK = s.BK;
+  if (threads) *threads = s.threads;
+  if (TM) *TM = s.TM;
+  if (TN) *TN = s.TN;
+  if (stages) *stages = s.stages;
+  return 0;
+}
+
+const char *sgemm_f32_version(void) { return "sgemm_f32 0.1.0 sm_103a"; }
+
+}  // extern "C"

@@ -1,0 +1,129 @@
+/*
+ * sgemm_f32.h -- single-precision GEMM for one NVIDIA GB300 (sm_103a), C ABI.
+ *
+ * Operation (all entry points that compute):
+ *
+ *     C = alpha * A * B + beta * C
+ *
+ * on row-major float32 matrices with leading dimensions, the BLAS sgemm statement with
+ * op(A) = A and op(B) = B ("Lecture 4 - GPU Acceleration", CMU 11-868 notes, section 5.2
+ * "Interface"), written for row-major storage the way the kernels of "SGEMM six-level
+ * optimisation: evolution of the core code" index it (section 2, kernel K1: element (x, i)
+ * of A at A[x * K + i], generalised here to A[x * lda + i]).
+ *
+ * Layout
+ *   A is M x K, element (i, k) at A[i * lda + k], lda >= max(1, K).
+ *   B is K x N, element (k, j) at B[k * ldb + j], ldb >= max(1, N).
+ *   C is M x N, element (i, j) at C[i * ldc + j], ldc >= max(1, N).
+ *   A leading dimension is the distance in elements between the starts of two consecutive
+ *   rows, so a sub-matrix is passed as a pointer to its first element plus the parent's
+ *   ld, with no copy (same lecture, section 5.3). Elements outside the M x N view of C are
+ *   never written; elements outside the views of A and B are never read.
+ *   No alignment is required. 16-byte aligned B and C with ld a multiple of 4 take the
+ *   128-bit load / store paths; anything else takes 32-bit paths with the same results.
+ *
+ * Memory and ownership
+ *   A, B and C are device pointers owned by the caller (any memory the GPU can address with
+ *   a plain load: cudaMalloc, cudaMallocAsync, managed). The library keeps no pointer after
+ *   the call returns. C must not overlap A or B.
+ *   sgemm_f32 may allocate a split-K workspace with cudaMallocAsync on `stream` and free it
+ *   with cudaFreeAsync on the same stream before returning; sgemm_f32_workspace_size()
+ *   reports its size and sgemm_f32_ws() takes a caller-provided workspace instead.
+ *
+ * Asynchrony
+ *   Every compute call enqueues its kernels on `stream` (0 = the legacy default stream) and
+ *   returns without waiting. Results are visible after the stream is synchronised.
+ *
+ * Scalars and special cases (BLAS reference conventions)
+ *   alpha and beta are host floats passed by value.
+ *   M == 0 or N == 0: nothing is done, returns 0.
+ *   alpha == 0 or K == 0: A and B are not read; C = beta * C (C = 0 when beta == 0).
+ *   beta == 0: C is not read before it is written, so NaN or garbage in C does not
+ *   propagate.
+ *   NaN and Inf in A or B propagate by IEEE rules.
+ *
+ * Arithmetic
+ *   FP32 fused multiply-add on the CUDA cores (round to nearest even), FP32 accumulation.
+ *   The order of the k-sum differs from a sequential loop (per-thread k-sequential inside a
+ *   tile; split-K partial sums added in a fixed slice order). Results are deterministic:
+ *   the same call on the same device gives bitwise the same C.
+ *
+ * Return value (BLAS xerbla style: the first illegal argument, counted from 1)
+ *    0   success
+ *   -1   M < 0          -2   N < 0          -3   K < 0
+ *   -5   A == NULL while A must be read
+ *   -6   lda < max(1, K)
+ *   -7   B == NULL while B must be read
+ *   -8   ldb < max(1, N)
+ *   -10  C == NULL while M > 0 and N > 0
+ *   -11  ldc < max(1, N)
+ *   -13  (sgemm_f32_ws only) workspace too small or NULL while one is needed
+ *   >0   a cudaError_t from a launch or a stream-ordered allocation
+ *   Nothing is launched when an argument is illegal. The library never aborts or traps.
+ */
+#ifndef SGEMM_F32_H_
+#define SGEMM_F32_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Forward declaration compatible with cuda_runtime_api.h. */
+typedef struct CUstream_st *cudaStream_t;
+
+/* C = alpha * A * B + beta * C (row-major, FP32 FFMA path). See the file comment. */
+int sgemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+              int ldb, float beta, float *C, int ldc, cudaStream_t stream);
+
+/* Bytes of split-K workspace that sgemm_f32 would allocate for this problem on the
+ * current device (0 when the chosen plan needs none). Host-only query. Returns the same
+ * negative codes as sgemm_f32 for illegal shapes or leading dimensions, else 0. */
+int sgemm_f32_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
+                             size_t *bytes);
+
+/* Same as sgemm_f32, but any split-K workspace comes from the caller: `workspace` is a
+ * device buffer of `workspace_bytes` bytes, 16-byte aligned, not read before it is written
+ * and not used after the call's kernels finish. The call allocates nothing. */
+int sgemm_f32_ws(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                 int ldb, float beta, float *C, int ldc, void *workspace,
+                 size_t workspace_bytes, cudaStream_t stream);
+
+/* Launch plan chosen for a problem, for tests and tuning. Host-only: no CUDA call is made
+ * when num_sms > 0 (the SM count to plan for); num_sms == 0 asks the current device.
+ * alpha and beta matter only through their special values (alpha == 0, beta == 0, 1).
+ * Outputs (any may be NULL):
+ *   variant  tile configuration index (0 .. sgemm_f32_num_variants() - 1), -1 when no
+ *            GEMM kernel runs (empty problem or beta-scale only)
+ *   split    number of K slices (1 = no split-K)
+ *   launches kernels enqueued by one sgemm_f32 call
+ *   ws_bytes split-K workspace bytes
+ * Returns the same negative codes as sgemm_f32 for illegal arguments, else 0. */
+int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta,
+                   int num_sms, int *variant, int *split, int *launches, size_t *ws_bytes);
+
+/* Tile configurations compiled into the library, for tests and tuning. */
+int sgemm_f32_num_variants(void);
+
+/* Describe variant v: CTA tile BM x BN x BK, threads per CTA, per-thread TM x TN
+ * accumulator tile, pipeline stages. Returns 0, or -1 if v is out of range. */
+int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *TM,
+                           int *TN, int *stages);
+
+/* sgemm_f32 with the plan forced: `variant` in [0, sgemm_f32_num_variants()) and
+ * `split` >= 1 (clamped so that every slice holds at least one K tile). Pass variant = -1
+ * and split = 0 for the automatic plan. For tests and tuning sweeps; results satisfy the
+ * same contract as sgemm_f32. Returns -14 for an out-of-range variant. */
+int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
+                     const float *B, int ldb, float beta, float *C, int ldc, int variant,
+                     int split, cudaStream_t stream);
+
+/* Library version string, e.g. "sgemm_f32 0.1.0 sm_103a". */
+const char *sgemm_f32_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SGEMM_F32_H_ */

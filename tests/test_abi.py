@@ -1,0 +1,126 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol its header
+declares, rejects illegal arguments before touching the GPU, and plans launches as
+intended. No compute call is made here (there may be no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import dense_fp32_matrix_08_gb300 as sg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMS = 152  # SM count planned for (GB300)
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared_functions()
+    assert "sgemm_f32" in names and len(names) >= 8
+    lib = ctypes.CDLL(sg.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+    assert set(sg.EXPORTED) <= set(names)
+
+
+def test_version():
+    assert sg.sgemm_f32_version().startswith("sgemm_f32 ")
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -1),
+    ((4, -1, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -2),
+    ((4, 4, -1, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -3),
+    ((4, 4, 4, 1.0, None, 4, 8, 4, 0.0, 8, 4), -5),
+    ((4, 4, 4, 1.0, 8, 3, 8, 4, 0.0, 8, 4), -6),
+    ((4, 4, 4, 1.0, 8, 4, None, 4, 0.0, 8, 4), -7),
+    ((4, 4, 4, 1.0, 8, 4, 8, 3, 0.0, 8, 4), -8),
+    ((4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, None, 4), -10),
+    ((4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 3), -11),
+    ((4, 4, 0, 1.0, 8, 0, 8, 4, 0.0, 8, 4), -6),     # lda >= max(1, K)
+    ((-1, -1, -1, 1.0, None, 0, None, 0, 0.0, None, 0), -1),  # first illegal one wins
+])
+def test_illegal_arguments(args, code):
+    # pointer 8 is never dereferenced: validation fails before any CUDA call
+    assert sg.sgemm_f32(*args, stream=0) == code
+    assert sg.sgemm_f32_ws(*args, 0, 0, stream=0) == code
+    assert sg.sgemm_f32_forced(*args, -1, 0, stream=0) == code
+
+
+def test_null_ab_allowed_when_not_read():
+    # M == 0 or N == 0 returns 0 before any CUDA call
+    assert sg.sgemm_f32(0, 4, 4, 1.0, None, 4, None, 4, 0.0, None, 4, stream=0) == 0
+    assert sg.sgemm_f32(4, 0, 4, 1.0, None, 4, None, 1, 0.0, None, 1, stream=0) == 0
+    # alpha == 0: A and B may be NULL (validation passes; plan says beta-scale only)
+    p = sg.sgemm_f32_plan(4, 4, 4, 4, 4, 4, alpha=0.0, beta=2.0, num_sms=SMS)
+    assert p["status"] == 0 and p["variant"] == -1 and p["launches"] == 1
+    p = sg.sgemm_f32_plan(4, 4, 4, 4, 4, 4, alpha=0.0, beta=1.0, num_sms=SMS)
+    assert p["launches"] == 0
+
+
+def test_forced_variant_out_of_range():
+    n = sg.sgemm_f32_num_variants()
+    assert sg.sgemm_f32_forced(4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4, n, 1, stream=0) == -14
+    assert sg.sgemm_f32_forced(4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4, -2, 1, stream=0) == -14
+
+
+def test_variant_table():
+    n = sg.sgemm_f32_num_variants()
+    assert n >= 5
+    for v in range(n):
+        info = sg.sgemm_f32_variant_info(v)
+        assert info["BM"] % 16 == 0 and info["BN"] % 16 == 0 and info["BK"] % 8 == 0
+        assert info["TM"] * info["TN"] >= 32 and info["threads"] % 32 == 0
+        # the CTA tile is exactly covered by its threads' accumulator tiles
+        assert info["BM"] * info["BN"] == info["threads"] * info["TM"] * info["TN"]
+    assert sg.sgemm_f32_variant_info(n) is None
+    big = sg.sgemm_f32_variant_info(0)
+    assert big["TM"] * big["TN"] >= 64  # at least an 8x8 register outer product
+
+
+def _plan(M, N, K, beta=1.0):
+    p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, beta, SMS)
+    assert p["status"] == 0
+    return p
+
+
+def test_plan_headline_uses_large_tiles():
+    p = _plan(8192, 8192, 8192)
+    info = sg.sgemm_f32_variant_info(p["variant"])
+    assert info["TM"] * info["TN"] >= 64
+    assert p["launches"] == (2 if p["split"] > 1 else 1)
+
+
+def test_plan_thin_shapes_use_thin_tiles_and_split_k():
+    p = _plan(16, 4096, 4096)
+    info = sg.sgemm_f32_variant_info(p["variant"])
+    assert info["BM"] <= 16 and p["split"] > 1 and p["ws_bytes"] > 0
+    p = _plan(4096, 16, 8192)
+    info = sg.sgemm_f32_variant_info(p["variant"])
+    assert info["BN"] <= 16 and p["split"] > 1
+
+
+def test_plan_workspace_formula():
+    for shp in [(16, 4096, 4096), (4096, 16, 8192), (256, 256, 256), (1023, 1021, 4096)]:
+        M, N, K = shp
+        p = _plan(M, N, K)
+        if p["split"] > 1:
+            assert p["ws_bytes"] == 4 * p["split"] * M * ((N + 3) // 4 * 4)
+        else:
+            assert p["ws_bytes"] == 0
+
+
+def test_plan_split_never_exceeds_k_tiles():
+    for K in (1, 7, 16, 17, 33, 100):
+        p = _plan(64, 64, K)
+        info = sg.sgemm_f32_variant_info(p["variant"])
+        assert 1 <= p["split"] <= -(-K // info["BK"])

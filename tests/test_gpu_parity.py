@@ -1,0 +1,226 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU FP64 oracle.
+
+Every comparison is elementwise with the bound |C_gpu - R| <= 1e-4 (S + |beta c|) (see
+parity_util). Problems the oracle finishes in seconds are checked on every element; the
+full-size configurations are checked on sampled rows (first, last and random ones, so
+every ragged tile edge is included) plus random single elements, in the same launch
+configuration the benchmark times.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
+from parity_util import assert_bound, guard_intact, to_device_view
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import dense_fp32_matrix_08_gb300 as sg
+
+
+def _run(A, B, C, alpha, beta, lda=None, ldb=None, ldc=None, offs=(0, 0, 0), variant=-1,
+         split=0, fill_c=float("nan")):
+    """Upload, run sgemm_f32 (or the forced plan), download. Returns (C_out, guard_ok)."""
+    M, K = A.shape
+    N = B.shape[1]
+    dA, _ = to_device_view(A, lda, offs[0])
+    dB, _ = to_device_view(B, ldb, offs[1])
+    dC, bufC = to_device_view(C, ldc, offs[2], fill=fill_c)
+    if variant >= 0 or split > 0:
+        rc = sg.sgemm_f32_forced(M, N, K, alpha, dA.data_ptr() if dA.numel() else 0,
+                                 max(dA.stride(0), 1), dB.data_ptr() if dB.numel() else 0,
+                                 max(dB.stride(0), 1), beta,
+                                 dC.data_ptr() if dC.numel() else 0, max(dC.stride(0), 1),
+                                 variant, split)
+    else:
+        rc = sg.sgemm_f32(M, N, K, alpha, dA.data_ptr() if dA.numel() else 0,
+                          max(dA.stride(0), 1), dB.data_ptr() if dB.numel() else 0,
+                          max(dB.stride(0), 1), beta, dC.data_ptr() if dC.numel() else 0,
+                          max(dC.stride(0), 1))
+    assert rc == 0, f"sgemm returned {rc}"
+    torch.cuda.synchronize()
+    return dC.cpu(), guard_intact(bufC, dC, fill_c)
+
+
+# --------------------------------------------------------------------------------------
+# The benchmark configurations.
+
+SMALL = ["sgemm_256cube", "sgemm_1024cube", "sgemm_4099x3001x777_ragged",
+         "sgemm_16x4096x4096_thin_m", "sgemm_4096x16x8192_thin_n"]
+LARGE = ["sgemm_4096cube", "sgemm_4097cube_unaligned", "sgemm_8192cube",
+         "sgemm_8192x14336x4096"]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_config_full(name):
+    w = BY_NAME[name]
+    A, B, C = workload_inputs(w)
+    out, guard = _run(A, B, C, w.alpha, w.beta)
+    assert guard, "wrote outside the C view"
+    R, S = oracle.sgemm_f64(A, B, C, w.alpha, w.beta)
+    assert_bound(out.numpy(), R, S, w.beta, C.numpy(), name)
+
+
+def _sample_rows(M, BMs=(16, 64, 128, 256), n_random=24, seed=0):
+    rows = {0, 1, M - 2, M - 1}
+    for bm in BMs:  # last full tile row and the ragged tail of every tile height
+        t = (M // bm) * bm
+        rows.update(r for r in (t - 1, t, t + 1) if 0 <= r < M)
+    rng = np.random.default_rng(seed)
+    rows.update(rng.integers(0, M, n_random).tolist())
+    return np.array(sorted(rows))
+
+
+@pytest.mark.parametrize("name", LARGE)
+def test_config_sampled(name):
+    w = BY_NAME[name]
+    A, B, C = workload_inputs(w)
+    out, guard = _run(A, B, C, w.alpha, w.beta, fill_c=0.0)
+    assert guard
+    rows = _sample_rows(w.M)
+    R, S = oracle.sgemm_f64_rows(A, B, C, w.alpha, w.beta, rows)
+    assert_bound(out.numpy()[rows], R, S, w.beta, C.numpy()[rows], name + " rows")
+    rng = np.random.default_rng(1)
+    ii = rng.integers(0, w.M, 4000)
+    jj = rng.integers(0, w.N, 4000)
+    Re, Se = oracle.sgemm_f64_entries(A, B, C, w.alpha, w.beta, ii, jj)
+    assert_bound(out.numpy()[ii, jj], Re, Se, w.beta, C.numpy()[ii, jj], name + " entries")
+
+
+# --------------------------------------------------------------------------------------
+# Every variant, aligned and unaligned, with and without split-K, across ragged tiles.
+
+def _variants():
+    return list(range(sg.sgemm_f32_num_variants())) if torch.cuda.is_available() else []
+
+
+RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
+          (255, 31, 100), (16, 300, 257), (300, 16, 129), (257, 255, 1)]
+
+
+@pytest.mark.parametrize("variant", range(5))
+@pytest.mark.parametrize("split", [1, 3])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_variant_ragged(variant, split, aligned):
+    for (M, N, K) in RAGGED:
+        A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
+        if aligned:
+            lds, offs = (None, None, None), (0, 0, 0)
+        else:  # odd leading dimensions and odd element offsets: 32-bit paths everywhere
+            lds, offs = (K + 1, N + 3, N + 5), (1, 3, 5)
+        out, guard = _run(A, B, C, 0.75, -1.25, *lds, offs=offs, variant=variant,
+                          split=split)
+        assert guard, (M, N, K)
+        R, S = oracle.sgemm_f64(A, B, C, 0.75, -1.25)
+        assert_bound(out.numpy(), R, S, -1.25, C.numpy(), f"v{variant} s{split} {M,N,K}")
+
+
+def test_ragged_sweep_auto_plan():
+    """Small M, N, K around tile edges under the automatic plan."""
+    edges = [1, 2, 3, 5, 8, 15, 16, 17, 127, 128, 129, 255, 256, 257]
+    rng = np.random.default_rng(3)
+    for t in range(60):
+        M, N, K = (int(rng.choice(edges)) for _ in range(3))
+        A, B, C = make_inputs(M, N, K, seed=100 + t)
+        out, guard = _run(A, B, C, 1.0, 0.5)
+        assert guard, (M, N, K)
+        R, S = oracle.sgemm_f64(A, B, C, 1.0, 0.5)
+        assert_bound(out.numpy(), R, S, 0.5, C.numpy(), f"auto {M,N,K}")
+
+
+# --------------------------------------------------------------------------------------
+# BLAS special cases and contract details.
+
+def test_beta_zero_does_not_read_c():
+    A, B, _ = make_inputs(70, 90, 33, seed=5)
+    C = torch.full((70, 90), float("nan"))
+    out, _ = _run(A, B, C, 1.5, 0.0)
+    R, S = oracle.sgemm_f64(A, B, None, 1.5, 0.0)
+    assert torch.isfinite(out).all()
+    assert_bound(out.numpy(), R, S, 0.0, None, "beta=0")
+
+
+def test_alpha_zero_does_not_read_ab():
+    A = torch.full((40, 30), float("nan"))
+    B = torch.full((30, 50), float("nan"))
+    _, _, C = make_inputs(40, 50, 30, seed=6)
+    out, _ = _run(A, B, C, 0.0, -2.0)
+    assert torch.equal(out, C * -2.0)
+    out0, _ = _run(A, B, C, 0.0, 0.0)
+    assert torch.equal(out0, torch.zeros_like(C))
+    out1, _ = _run(A, B, C, 0.0, 1.0)
+    assert torch.equal(out1, C)
+
+
+def test_k_zero():
+    A = torch.zeros((20, 0))
+    B = torch.zeros((0, 24))
+    _, _, C = make_inputs(20, 24, 1, seed=7)
+    out, _ = _run(A, B, C, 1.0, 3.0)
+    assert torch.equal(out, C * 3.0)
+
+
+def test_empty_m_n_is_noop():
+    for M, N in ((0, 5), (5, 0), (0, 0)):
+        assert sg.sgemm_f32(M, N, 4, 1.0, 0, 4, 0, max(N, 1), 0.0, 0, max(N, 1)) == 0
+
+
+def test_fp32_fidelity_exact():
+    """A = 1 + 2^-15 (not representable in TF32), B = 1, K = 256: the exact sum is
+    256 + 2^-7, which FP32 FFMA reaches exactly; a TF32 path would give 256."""
+    M, N, K = 64, 64, 256
+    A = torch.full((M, K), 1.0 + 2.0 ** -15)
+    B = torch.ones((K, N))
+    C = torch.zeros((M, N))
+    for v in _variants():
+        out, _ = _run(A, B, C, 1.0, 0.0, variant=v, split=1)
+        assert torch.all(out == 256.0 + 2.0 ** -7), f"variant {v}"
+
+
+def test_deterministic_and_ws_entry_match():
+    A, B, C = make_inputs(1000, 1000, 1000, seed=8)
+    o1, _ = _run(A, B, C, 1.0, 1.0)
+    o2, _ = _run(A, B, C, 1.0, 1.0)
+    assert torch.equal(o1, o2)
+    M = N = K = 1000
+    dA, _ = to_device_view(A)
+    dB, _ = to_device_view(B)
+    dC, _ = to_device_view(C)
+    rc, nbytes = sg.sgemm_f32_workspace_size(M, N, K, K, N, N)
+    assert rc == 0
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device="cuda")
+    assert sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, dC, N, ws.data_ptr(),
+                           ws.numel()) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(dC.cpu(), o1)
+    if nbytes:
+        dC2, _ = to_device_view(C)
+        assert sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, dC2, N, ws.data_ptr(),
+                               nbytes - 1) == -13
+
+
+def test_illegal_arguments_launch_nothing():
+    A, B, C = make_inputs(8, 8, 8, seed=9)
+    dA, _ = to_device_view(A)
+    dB, _ = to_device_view(B)
+    dC, _ = to_device_view(C)
+    before = dC.clone()
+    assert sg.sgemm_f32(8, 8, 8, 1.0, dA, 7, dB, 8, 0.0, dC, 8) == -6
+    assert sg.sgemm_f32(8, 8, 8, 1.0, dA, 8, dB, 7, 0.0, dC, 8) == -8
+    assert sg.sgemm_f32(8, 8, 8, 1.0, dA, 8, dB, 8, 0.0, dC, 7) == -11
+    assert sg.sgemm_f32(8, 8, 8, 1.0, None, 8, dB, 8, 0.0, dC, 8) == -5
+    torch.cuda.synchronize()
+    assert torch.equal(dC, before)
+
+
+def test_torch_tensor_helper_and_streams():
+    A, B, C = make_inputs(300, 200, 100, seed=10)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        dA, dB, dC = A.cuda(), B.cuda(), C.cuda()
+        sg.sgemm(dA, dB, dC, 2.0, 0.5)
+    s.synchronize()
+    R, S = oracle.sgemm_f64(A, B, C, 2.0, 0.5)
+    assert_bound(dC.cpu().numpy(), R, S, 0.5, C.numpy(), "stream")
