@@ -49,7 +49,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_ws.argtypes = gemm + [vp, sz, vp]
     L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
-    L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, psz]
+    L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
     L.sgemm_f32_variant_info.argtypes = [i] + [pi] * 7
     L.sgemm_f32_version.argtypes = []
@@ -113,12 +113,13 @@ def sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc) -> tuple[int, int]:
 
 
 def sgemm_f32_plan(M, N, K, lda, ldb, ldc, alpha=1.0, beta=0.0, num_sms=0) -> dict:
-    v, s, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
+    v, s, mt, n = ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0), ctypes.c_int(0)
     ws = ctypes.c_size_t(0)
     rc = lib.sgemm_f32_plan(M, N, K, lda, ldb, ldc, alpha, beta, num_sms, ctypes.byref(v),
-                            ctypes.byref(s), ctypes.byref(n), ctypes.byref(ws))
-    return {"status": rc, "variant": v.value, "split": s.value, "launches": n.value,
-            "ws_bytes": ws.value}
+                            ctypes.byref(s), ctypes.byref(mt), ctypes.byref(n),
+                            ctypes.byref(ws))
+    return {"status": rc, "variant": v.value, "split": s.value, "main_tiles": mt.value,
+            "launches": n.value, "ws_bytes": ws.value}
 
 
 def sgemm_f32_num_variants() -> int:

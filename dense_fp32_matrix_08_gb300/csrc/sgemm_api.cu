@@ -11,51 +11,16 @@
 
 #include "../../include/sgemm_f32.h"
 #include "sgemm_aux.cuh"
-#include "sgemm_ffma.cuh"
 #include "sgemm_plan.h"
+#include "sgemm_variants.cuh"
 
 namespace sgemm {
 
-// ------------------------------------------------------------------------------------
-// Tile configurations. Their shapes are also listed, without CUDA, in sgemm_plan.h
-// (kVariants); a static_assert below keeps the two in step.
-using V0 = TileConfig<128, 256, 16, 64, 64, 16, 8, 3, 1>;  // large tiles, 128 acc/thread
-using V1 = TileConfig<128, 128, 16, 32, 64, 8, 8, 4, 2>;   // 8x8 per thread, 2 CTAs/SM
-using V2 = TileConfig<64, 64, 16, 32, 32, 8, 4, 4, 4>;     // small tiles for small problems
-using V3 = TileConfig<16, 256, 32, 16, 64, 8, 4, 3, 2>;    // thin M (M <= 16 per tile)
-using V4 = TileConfig<256, 16, 32, 64, 16, 8, 4, 3, 2>;    // thin N (N <= 16 per tile)
-
-template <class Cfg>
-constexpr bool matches(const VariantShape &s) {
-  return s.BM == Cfg::BM && s.BN == Cfg::BN && s.BK == Cfg::BK && s.threads == Cfg::NT &&
-         s.TM == Cfg::TM && s.TN == Cfg::TN && s.stages == Cfg::STAGES &&
-         s.min_blocks == Cfg::MIN_BLOCKS && s.smem_bytes == Cfg::SMEM_BYTES;
-}
-static_assert(kNumVariants == 5, "variant table size");
-static_assert(matches<V0>(kVariants[0]) && matches<V1>(kVariants[1]) &&
-                  matches<V2>(kVariants[2]) && matches<V3>(kVariants[3]) &&
-                  matches<V4>(kVariants[4]),
-              "sgemm_plan.h variant table out of step with the kernel configurations");
-
-using KernelFn = void (*)(const GemmParams);
-
-struct VariantKernels {
-  KernelFn k[2][2];  // [vec_b][split]
-  int threads;
-  int smem;
-};
-
-template <class Cfg>
-constexpr VariantKernels make_kernels() {
-  return VariantKernels{{{sgemm_ffma_kernel<Cfg, false, false>, sgemm_ffma_kernel<Cfg, false, true>},
-                         {sgemm_ffma_kernel<Cfg, true, false>, sgemm_ffma_kernel<Cfg, true, true>}},
-                        Cfg::NT,
-                        Cfg::SMEM_BYTES};
-}
-
 static const VariantKernels kKernels[kNumVariants] = {
-    make_kernels<V0>(), make_kernels<V1>(), make_kernels<V2>(), make_kernels<V3>(),
-    make_kernels<V4>()};
+#define SGEMM_KERNELS_ENTRY(v) variant_kernels<v>(),
+    SGEMM_FOR_EACH_VARIANT(SGEMM_KERNELS_ENTRY)
+#undef SGEMM_KERNELS_ENTRY
+};
 
 // ------------------------------------------------------------------------------------
 // Per-device one-time setup: opt every kernel into its dynamic shared memory and cache
@@ -79,10 +44,8 @@ static cudaError_t device_setup(int *num_sms) {
     cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     for (int v = 0; v < kNumVariants && err == cudaSuccess; ++v)
       for (int a = 0; a < 2 && err == cudaSuccess; ++a)
-        for (int b = 0; b < 2 && err == cudaSuccess; ++b)
-          err = cudaFuncSetAttribute(kKernels[v].k[a][b],
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kKernels[v].smem);
+        err = cudaFuncSetAttribute(kKernels[v].k[a], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kKernels[v].smem);
     st.num_sms = sms;
     st.err = err;
   });
@@ -126,23 +89,24 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   p.C = C;
   p.ldc = pr.ldc;
   p.ws = ws;
-  p.ldw = workspace_ld(pr.N);
+  p.main_tiles = pl.main_tiles;
+  p.split = pl.split;
   p.k_per_split = pl.k_per_split;
   p.tiles_m = pl.tiles_m;
   p.tiles_n = pl.tiles_n;
   p.group_m = pl.group_m;
   p.vec_c = vec_c ? 1 : 0;
   const bool vec_b = (pr.ldb % 4 == 0) && aligned16(B);
-  const bool split = pl.split > 1;
-  if ((long long)pl.tiles_m * pl.tiles_n > 0x7fffffffLL) return (int)cudaErrorInvalidConfiguration;
-  dim3 grid((unsigned)(pl.tiles_m * pl.tiles_n), (unsigned)pl.split, 1);
-  kKernels[pl.variant].k[vec_b][split]<<<grid, vs.threads, vs.smem_bytes, stream>>>(p);
+  if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
+  kKernels[pl.variant].k[vec_b]<<<pl.ctas, vs.threads, vs.smem_bytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
-  if (split) {
-    const long long work = (long long)pr.M * ((pr.N + 3) / 4);
-    splitk_reduce_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
-        ws, p.ldw, pl.split, pr.M, pr.N, alpha, beta, C, pr.ldc, vec_c ? 1 : 0);
+  const long long tail_tiles = (long long)pl.tiles_m * pl.tiles_n - pl.main_tiles;
+  if (tail_tiles > 0) {
+    const long long work = (long long)tail_tiles * vs.BM * (vs.BN / 4);
+    tail_reduce_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+        ws, pl.main_tiles, (int)tail_tiles, pl.split, vs.BM, vs.BN, pl.tiles_m, pl.tiles_n,
+        pl.group_m, pr.M, pr.N, alpha, beta, C, pr.ldc, vec_c ? 1 : 0);
     e = cudaGetLastError();
   }
   return (int)e;
@@ -210,11 +174,12 @@ int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
 int sgemm_f32_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
                              size_t *bytes) {
   return sgemm_f32_plan(M, N, K, lda, ldb, ldc, 1.0f, 1.0f, 0, nullptr, nullptr, nullptr,
-                        bytes);
+                        nullptr, bytes);
 }
 
 int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta,
-                   int num_sms, int *variant, int *split, int *launches, size_t *ws_bytes) {
+                   int num_sms, int *variant, int *split, int *main_tiles, int *launches,
+                   size_t *ws_bytes) {
   Problem pr{M, N, K, lda, ldb, ldc};
   int rc = validate(pr, alpha, true, true, true);
   if (rc != 0) return rc;
@@ -225,14 +190,12 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
   Plan pl;
   if (M == 0 || N == 0) {
     pl.variant = -1;
-    pl.split = 1;
-    pl.launches = 0;
-    pl.ws_bytes = 0;
   } else {
     pl = make_plan(pr, alpha, beta, num_sms, -1, 0);
   }
   if (variant) *variant = pl.variant;
   if (split) *split = pl.split;
+  if (main_tiles) *main_tiles = pl.main_tiles;
   if (launches) *launches = pl.launches;
   if (ws_bytes) *ws_bytes = pl.ws_bytes;
   return 0;

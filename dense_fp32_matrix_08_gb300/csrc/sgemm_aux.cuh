@@ -5,6 +5,8 @@
 
 #include <cuda_runtime.h>
 
+#include "sgemm_ffma.cuh"
+
 namespace sgemm {
 
 // C = beta * C over an M x N view (beta == 0 writes zeros without reading C). This is the
@@ -34,28 +36,39 @@ __global__ void scale_c_kernel(float *__restrict__ C, long long ldc, int M, int 
   }
 }
 
-// Split-K finish: C = alpha * sum_{s < splits} ws[s] + beta * C, the slices added in
-// ascending s so that results are deterministic. ws is [splits][M][ldw], ldw % 4 == 0.
-__global__ void splitk_reduce_kernel(const float *__restrict__ ws, long long ldw, int splits,
-                                     int M, int N, float alpha, float beta,
-                                     float *__restrict__ C, long long ldc, int vec) {
-  const long long groups_per_row = (N + 3) / 4;
-  const long long total = (long long)M * groups_per_row;
-  const long long slice = (long long)M * ldw;
+// Split-K finish for the tiles the GEMM kernel computed in K slices (CTA main_tiles + u
+// wrote slice u % split of tile main_tiles + u / split to ws[u], a BM x BN row-major
+// partial tile): C = alpha * sum_s partial_s + beta * C, slices added in ascending order
+// so that results are deterministic. One thread handles 4 consecutive columns of a row.
+__global__ void tail_reduce_kernel(const float *__restrict__ ws, int main_tiles, int tail_tiles,
+                                   int split, int BM, int BN, int tiles_m, int tiles_n,
+                                   int group_m, int M, int N, float alpha, float beta,
+                                   float *__restrict__ C, long long ldc, int vec) {
+  const int quads = BN / 4;
+  const long long per_tile = (long long)BM * quads;
+  const long long total = (long long)tail_tiles * per_tile;
+  const long long tile_elems = (long long)BM * BN;
   for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
        g += (long long)gridDim.x * blockDim.x) {
-    const long long row = g / groups_per_row;
-    const int col = (int)(g - row * groups_per_row) * 4;
-    const float *src = ws + row * ldw + col;
+    const int t = (int)(g / per_tile);
+    const int e = (int)(g - (long long)t * per_tile);
+    const int r = e / quads;
+    const int c4 = (e - r * quads) * 4;
+    int tm, tn;
+    tile_coords(main_tiles + t, tiles_m, tiles_n, group_m, tm, tn);
+    const int row = tm * BM + r;
+    const int col = tn * BN + c4;
+    if (row >= M || col >= N) continue;
+    const float *src = ws + (long long)t * split * tile_elems + (long long)r * BN + c4;
     float4 s = *reinterpret_cast<const float4 *>(src);
-    for (int k = 1; k < splits; ++k) {
-      const float4 t = *reinterpret_cast<const float4 *>(src + k * slice);
-      s.x += t.x;
-      s.y += t.y;
-      s.z += t.z;
-      s.w += t.w;
+    for (int k = 1; k < split; ++k) {
+      const float4 q = *reinterpret_cast<const float4 *>(src + k * tile_elems);
+      s.x += q.x;
+      s.y += q.y;
+      s.z += q.z;
+      s.w += q.w;
     }
-    float *dst = C + row * ldc + col;
+    float *dst = C + (long long)row * ldc + col;
     if (vec && col + 3 < N) {
       float4 out;
       if (beta != 0.0f) {
@@ -70,8 +83,8 @@ __global__ void splitk_reduce_kernel(const float *__restrict__ ws, long long ldw
       *reinterpret_cast<float4 *>(dst) = out;
     } else {
       const float v[4] = {s.x, s.y, s.z, s.w};
-      for (int e = 0; e < 4 && col + e < N; ++e)
-        dst[e] = (beta != 0.0f) ? fmaf(alpha, v[e], beta * dst[e]) : alpha * v[e];
+      for (int q = 0; q < 4 && col + q < N; ++q)
+        dst[q] = (beta != 0.0f) ? fmaf(alpha, v[q], beta * dst[q]) : alpha * v[q];
     }
   }
 }

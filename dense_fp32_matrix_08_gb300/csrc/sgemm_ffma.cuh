@@ -29,6 +29,8 @@
 #pragma once
 
 #include <cstdint>
+#include <type_traits>
+
 #include <cuda_runtime.h>
 
 namespace sgemm {
@@ -42,9 +44,15 @@ struct GemmParams {
   long long ldb;
   float *C;
   long long ldc;
-  float *ws;          // split-K partials, [split][M][ldw]; unused when split == 1
-  long long ldw;      // row stride of the partials (N rounded up to 4)
-  int k_per_split;    // K elements per slice, a multiple of BK
+  // Work decomposition. CTAs 0 .. main_tiles-1 compute whole tiles (tile = CTA index, all
+  // of K) and write C. The remaining tiles are split along K into `split` slices of
+  // k_per_split elements; CTA main_tiles + u handles slice u % split of tile
+  // main_tiles + u / split and writes its BM x BN partial tile to ws[u] (BM * BN floats,
+  // row-major). A reduction kernel then finishes those tiles in slice order.
+  float *ws;
+  int main_tiles;
+  int split;
+  int k_per_split;    // multiple of BK
   int tiles_m, tiles_n;
   int group_m;        // tile-rows per L2 group
   int vec_c;          // 1: C is 16-byte aligned with ldc % 4 == 0 (128-bit epilogue)
@@ -84,18 +92,28 @@ __device__ __forceinline__ void cp_async_wait() {
 // Tile configuration. All sizes are compile-time; static_asserts spell out which
 // combinations are legal (the template-parameter legality idea of "GPU GEMM optimisation,
 // part 2", autotuning section).
+//
+// MODE selects how the register outer product is issued:
+//   0  scalar FFMA, one accumulator per instruction;
+//   1  packed FFMA2 (fma.rn.f32x2) on accumulator pairs along N, the A value broadcast
+//      into both halves of a register pair in registers;
+//   2  packed FFMA2 with the broadcast done by the copy: every A element is stored twice in
+//      shared memory, so 128-bit fragment loads return ready-made {a_i, a_i, a_i+1, a_i+1}.
+// FFMA2 does the same FP32 work per pipe cycle as FFMA but needs half the issue slots,
+// which leaves room for the fragment loads, copies and address arithmetic to overlap.
 template <int BM_, int BN_, int BK_, int WM_, int WN_, int TM_, int TN_, int STAGES_,
-          int MIN_BLOCKS_>
+          int MIN_BLOCKS_, int MODE_ = 0>
 struct TileConfig {
   static constexpr int BM = BM_, BN = BN_, BK = BK_;
   static constexpr int WM = WM_, WN = WN_, TM = TM_, TN = TN_;
-  static constexpr int STAGES = STAGES_, MIN_BLOCKS = MIN_BLOCKS_;
+  static constexpr int STAGES = STAGES_, MIN_BLOCKS = MIN_BLOCKS_, MODE = MODE_;
+  static constexpr int AW = (MODE == 2) ? 2 : 1;  // floats stored per A element
   static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
   static constexpr int NWARPS = WARPS_M * WARPS_N;
   static constexpr int NT = NWARPS * 32;
   static constexpr int LM = WM / TM, LN = WN / TN;  // lanes along M and N in a warp
   static constexpr int FM = TM / 4, FN = TN / 4;    // float4 fragments per k step
-  static constexpr int A_STAGE = BK * BM, B_STAGE = BK * BN;  // floats per stage
+  static constexpr int A_STAGE = BK * BM * AW, B_STAGE = BK * BN;  // floats per stage
   static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
   // A copy: one warp instruction moves an 8 (k) x 4 (m) block.
   static constexpr int A_BLOCKS = (BK / 8) * (BM / 4);
@@ -105,7 +123,7 @@ struct TileConfig {
   static constexpr int B_ITERS_VEC = B_CHUNKS / NT;
   static constexpr int B_ITERS_SCALAR = BK * BN / NT;
   // XOR swizzle of As chunk index: low bits flipped by k.
-  static constexpr int SWZ = (BM / 4 >= 8) ? 7 : (BM / 4 - 1);
+  static constexpr int SWZ = (BM * AW / 4 >= 8) ? 7 : (BM * AW / 4 - 1);
 
   static_assert(BM % WM == 0 && BN % WN == 0, "warp tiles must divide the CTA tile");
   static_assert(LM * LN == 32, "a warp is 32 lanes");
@@ -118,9 +136,48 @@ struct TileConfig {
   static_assert((BK * BN) % NT == 0, "B 4-byte copies must tile");
   static_assert(STAGES >= 2, "need at least double buffering");
   static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA on sm_103a");
+  static_assert(MODE >= 0 && MODE <= 2, "unknown MODE");
+  static_assert(MODE != 2 || BM % 32 == 0, "duplicated A layout needs BM % 32 == 0");
 };
 
+// Physical float index, inside one As row (fixed k), of logical column `x`:
+//   MODE 0/1: x = m, one float per A row m.
+//   MODE 2:   every A row m occupies two floats. Rows (2p, 2p+1) share one 16-byte chunk
+//             {a_2p, a_2p, a_2p+1, a_2p+1}; chunk (p & 1) * (BM / 4) + (p >> 1) holds them,
+//             so the two chunks a thread needs for rows 4l..4l+3 sit at l and BM/4 + l and
+//             the lanes of a warp read consecutive chunks.
+// The chunk index is then XOR-swizzled with k.
+template <class Cfg>
+__device__ __forceinline__ int a_phys(int k, int m, int dup) {
+  if constexpr (Cfg::MODE == 2) {
+    const int pr = m >> 1;
+    const int chunk = (pr & 1) * (Cfg::BM / 4) + (pr >> 1);
+    return ((chunk ^ (k & Cfg::SWZ)) << 2) | ((m & 1) << 1) | dup;
+  } else {
+    return (((m >> 2) ^ (k & Cfg::SWZ)) << 2) | (m & 3);
+  }
+}
+
+// d = a * b + c on register pairs {lo, hi} (two independent FP32 FMAs, round to nearest).
+__device__ __forceinline__ void ffma2(unsigned long long &d, unsigned long long a,
+                                      unsigned long long b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;\n" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ unsigned long long pack2(float lo, float hi) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};\n" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+
+__device__ __forceinline__ float2 unpack2(unsigned long long v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;\n" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+
 // Grouped tile order: GROUP_M tile-rows are swept column by column before moving on.
+// Tile index -> (tile row, tile column); shared by the GEMM and split-K reduce kernels.
 __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, int group_m,
                                             int &tm, int &tn) {
   const int group_size = group_m * tiles_n;
@@ -132,16 +189,17 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
   tn = in_group / rows;
 }
 
-template <class Cfg, bool VEC_B, bool SPLIT>
+template <class Cfg, bool VEC_B>
 __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const GemmParams p) {
   constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
   constexpr int TM = Cfg::TM, TN = Cfg::TN, LM = Cfg::LM, LN = Cfg::LN;
   constexpr int FM = Cfg::FM, FN = Cfg::FN, NT = Cfg::NT, NWARPS = Cfg::NWARPS;
-  constexpr int SWZ = Cfg::SWZ;
+  constexpr int MODE = Cfg::MODE;
+  constexpr int AROW = BM * Cfg::AW;  // floats per As row (one k)
 
   extern __shared__ __align__(128) float smem[];
-  float *As = smem;                               // [STAGES][BK][BM] swizzled
+  float *As = smem;                               // [STAGES][BK][AROW] swizzled
   float *Bs = smem + STAGES * Cfg::A_STAGE;       // [STAGES][BK][BN]
 
   const int tid = threadIdx.x;
@@ -152,13 +210,21 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
   const int lane_m = lane / LN;
   const int lane_n = lane % LN;
 
+  // which tile, which K range (see GemmParams)
+  const int w = blockIdx.x;
+  const bool partial = w >= p.main_tiles;
+  int tile = w, k_begin = 0, k_end = p.K;
+  if (partial) {
+    const int u = w - p.main_tiles;
+    tile = p.main_tiles + u / p.split;
+    k_begin = (u % p.split) * p.k_per_split;
+    k_end = min(p.K, k_begin + p.k_per_split);
+  }
   int tm, tn;
-  tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
   const int m0 = tm * BM;
   const int n0 = tn * BN;
 
-  const int k_begin = SPLIT ? blockIdx.y * p.k_per_split : 0;
-  const int k_end = SPLIT ? min(p.K, k_begin + p.k_per_split) : p.K;
   const int KT = (k_end - k_begin + BK - 1) / BK;
 
   // ---- per-thread copy coordinates -------------------------------------------------
@@ -175,8 +241,8 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
 
   auto load_tile = [&](int kt, int slot) {
     const int k0 = k_begin + kt * BK;
-    // A, transposed on the fly into As[slot][k][swizzled m]
-    float *as = As + slot * Cfg::A_STAGE;
+    // A, transposed on the fly into As[slot][k][a_phys(m)]
+    float *as = As + slot * Cfg::A_STAGE + a_k * AROW;
     const int kg = k0 + a_k;
     const bool k_ok = kg < k_end;
 #pragma unroll
@@ -185,8 +251,9 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
       const int mg = m0 + m;
       const bool ok = k_ok && (mg < p.M);
       const float *src = ok ? p.A + (long long)mg * p.lda + kg : p.A;
-      const int col = (((m >> 2) ^ (a_k & SWZ)) << 2) | (m & 3);
-      cp_async_4(smem_addr(as + a_k * BM + col), src, ok ? 4 : 0);
+      cp_async_4(smem_addr(as + a_phys<Cfg>(a_k, m, 0)), src, ok ? 4 : 0);
+      if constexpr (MODE == 2)
+        cp_async_4(smem_addr(as + a_phys<Cfg>(a_k, m, 1)), src, ok ? 4 : 0);
     }
     float *bs = Bs + slot * Cfg::B_STAGE;
     if constexpr (VEC_B) {
@@ -215,11 +282,14 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     }
   };
 
-  float acc[TM][TN];
+  // Accumulators: scalar for MODE 0, register pairs along N for the FFMA2 modes.
+  constexpr int ACC_W = (MODE == 0) ? TN : TN / 2;
+  using acc_t = typename std::conditional<MODE == 0, float, unsigned long long>::type;
+  acc_t acc[TM][ACC_W];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
 #pragma unroll
-    for (int j = 0; j < TN; ++j) acc[i][j] = 0.0f;
+    for (int j = 0; j < ACC_W; ++j) acc[i][j] = 0;
 
   // ---- prologue: fill STAGES-1 slots ------------------------------------------------
 #pragma unroll
@@ -229,16 +299,25 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
   }
 
   // fragment addressing inside a stage
-  const int a_chunk0 = (warp_m * Cfg::WM + lane_m * 4) >> 2;  // chunk of sub-block 0
+  const int a_row0 = warp_m * Cfg::WM + lane_m * 4;  // first of the thread's rows (tile)
   const int b_col0 = warp_n * Cfg::WN + lane_n * 4;
 
-  float4 fa[2][FM], fb[2][FN];
+  // A fragments: MODE 0/1 -> FM float4 = TM values; MODE 2 -> 2*FM float4 = TM pairs.
+  constexpr int FA = (MODE == 2) ? 2 * FM : FM;
+  float4 fa[2][FA], fb[2][FN];
 
   auto load_frags = [&](const float *as, const float *bs, int k, int buf) {
+    const float *arow = as + k * AROW;
 #pragma unroll
     for (int r = 0; r < FM; ++r) {
-      const int chunk = a_chunk0 + r * LM;
-      fa[buf][r] = *reinterpret_cast<const float4 *>(as + k * BM + ((chunk ^ (k & SWZ)) << 2));
+      const int m = a_row0 + r * LM * 4;  // multiple of 4
+      if constexpr (MODE == 2) {
+        fa[buf][2 * r] = *reinterpret_cast<const float4 *>(arow + a_phys<Cfg>(k, m, 0));
+        fa[buf][2 * r + 1] =
+            *reinterpret_cast<const float4 *>(arow + a_phys<Cfg>(k, m + 2, 0));
+      } else {
+        fa[buf][r] = *reinterpret_cast<const float4 *>(arow + a_phys<Cfg>(k, m, 0));
+      }
     }
 #pragma unroll
     for (int c = 0; c < FN; ++c)
@@ -263,34 +342,93 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     for (int k = 0; k < BK; ++k) {
       const int cur = k & 1;
       if (k + 1 < BK) load_frags(as, bs, k + 1, cur ^ 1);
-      float a[TM], b[TN];
+      if constexpr (MODE == 0) {
+        float a[TM], b[TN];
 #pragma unroll
-      for (int r = 0; r < FM; ++r) {
-        a[r * 4 + 0] = fa[cur][r].x;
-        a[r * 4 + 1] = fa[cur][r].y;
-        a[r * 4 + 2] = fa[cur][r].z;
-        a[r * 4 + 3] = fa[cur][r].w;
+        for (int r = 0; r < FM; ++r) {
+          a[r * 4 + 0] = fa[cur][r].x;
+          a[r * 4 + 1] = fa[cur][r].y;
+          a[r * 4 + 2] = fa[cur][r].z;
+          a[r * 4 + 3] = fa[cur][r].w;
+        }
+#pragma unroll
+        for (int c = 0; c < FN; ++c) {
+          b[c * 4 + 0] = fb[cur][c].x;
+          b[c * 4 + 1] = fb[cur][c].y;
+          b[c * 4 + 2] = fb[cur][c].z;
+          b[c * 4 + 3] = fb[cur][c].w;
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      } else {
+        // b pairs (b_j, b_j+1) straight from the float4 fragments
+        unsigned long long b2[TN / 2];
+#pragma unroll
+        for (int c = 0; c < FN; ++c) {
+          b2[2 * c] = pack2(fb[cur][c].x, fb[cur][c].y);
+          b2[2 * c + 1] = pack2(fb[cur][c].z, fb[cur][c].w);
+        }
+        unsigned long long a2[TM];  // {a_i, a_i}
+#pragma unroll
+        for (int r = 0; r < FM; ++r) {
+          if constexpr (MODE == 2) {
+            a2[r * 4 + 0] = pack2(fa[cur][2 * r].x, fa[cur][2 * r].y);
+            a2[r * 4 + 1] = pack2(fa[cur][2 * r].z, fa[cur][2 * r].w);
+            a2[r * 4 + 2] = pack2(fa[cur][2 * r + 1].x, fa[cur][2 * r + 1].y);
+            a2[r * 4 + 3] = pack2(fa[cur][2 * r + 1].z, fa[cur][2 * r + 1].w);
+          } else {
+            a2[r * 4 + 0] = pack2(fa[cur][r].x, fa[cur][r].x);
+            a2[r * 4 + 1] = pack2(fa[cur][r].y, fa[cur][r].y);
+            a2[r * 4 + 2] = pack2(fa[cur][r].z, fa[cur][r].z);
+            a2[r * 4 + 3] = pack2(fa[cur][r].w, fa[cur][r].w);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+          for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], a2[i], b2[j]);
       }
-#pragma unroll
-      for (int c = 0; c < FN; ++c) {
-        b[c * 4 + 0] = fb[cur][c].x;
-        b[c * 4 + 1] = fb[cur][c].y;
-        b[c * 4 + 2] = fb[cur][c].z;
-        b[c * 4 + 3] = fb[cur][c].w;
-      }
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-#pragma unroll
-        for (int j = 0; j < TN; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
     }
   }
   cp_async_wait<0>();
 
   // ---- epilogue -----------------------------------------------------------------------
-  // Thread element (i, j) of acc sits at tile row warp_m*WM + (i/4)*LM*4 + lane_m*4 + i%4
-  // and tile column warp_n*WN + (j/4)*LN*4 + lane_n*4 + j%4.
-  const int row_base = m0 + warp_m * Cfg::WM + lane_m * 4;
-  const int col_base = n0 + warp_n * Cfg::WN + lane_n * 4;
+  // Thread element (i, j) of the tile sits at row warp_m*WM + (i/4)*LM*4 + lane_m*4 + i%4
+  // and column warp_n*WN + (j/4)*LN*4 + lane_n*4 + j%4.
+  auto acc4 = [&](int i, int c, float v[4]) {
+    if constexpr (MODE == 0) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = acc[i][c * 4 + e];
+    } else {
+      const float2 lo = unpack2(acc[i][c * 2]);
+      const float2 hi = unpack2(acc[i][c * 2 + 1]);
+      v[0] = lo.x;
+      v[1] = lo.y;
+      v[2] = hi.x;
+      v[3] = hi.y;
+    }
+  };
+  if (partial) {
+    // Whole partial tile, in range or not (out-of-range rows and columns hold zeros,
+    // since their loads were zero-filled); 16-byte stores, ws 16-byte aligned.
+    float *wt = p.ws + (long long)(w - p.main_tiles) * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+      const int r = a_row0 + (i >> 2) * LM * 4 + (i & 3);
+#pragma unroll
+      for (int c = 0; c < FN; ++c) {
+        float v[4];
+        acc4(i, c, v);
+        *reinterpret_cast<float4 *>(wt + r * BN + b_col0 + c * LN * 4) =
+            make_float4(v[0], v[1], v[2], v[3]);
+      }
+    }
+    return;
+  }
+  const int row_base = m0 + a_row0;
+  const int col_base = n0 + b_col0;
 #pragma unroll
   for (int i = 0; i < TM; ++i) {
     const int row = row_base + (i >> 2) * LM * 4 + (i & 3);
@@ -299,39 +437,26 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     for (int c = 0; c < FN; ++c) {
       const int col = col_base + c * LN * 4;
       if (col >= p.N) continue;
-      const float *v = &acc[i][c * 4];
-      if constexpr (SPLIT) {
-        // partial sums of this K slice; ldw % 4 == 0 and ws 16-byte aligned
-        float *dst = p.ws + ((long long)blockIdx.y * p.M + row) * p.ldw + col;
-        if (col + 3 < p.N) {
-          *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+      float v[4];
+      acc4(i, c, v);
+      float *dst = p.C + (long long)row * p.ldc + col;
+      if (p.vec_c && col + 3 < p.N) {
+        float4 out;
+        if (p.beta != 0.0f) {
+          const float4 old = *reinterpret_cast<const float4 *>(dst);
+          out.x = fmaf(p.alpha, v[0], p.beta * old.x);
+          out.y = fmaf(p.alpha, v[1], p.beta * old.y);
+          out.z = fmaf(p.alpha, v[2], p.beta * old.z);
+          out.w = fmaf(p.alpha, v[3], p.beta * old.w);
         } else {
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (col + e < p.N) dst[e] = v[e];
+          out = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
         }
+        *reinterpret_cast<float4 *>(dst) = out;
       } else {
-        float *dst = p.C + (long long)row * p.ldc + col;
-        if (p.vec_c && col + 3 < p.N) {
-          float4 out;
-          if (p.beta != 0.0f) {
-            const float4 old = *reinterpret_cast<const float4 *>(dst);
-            out.x = fmaf(p.alpha, v[0], p.beta * old.x);
-            out.y = fmaf(p.alpha, v[1], p.beta * old.y);
-            out.z = fmaf(p.alpha, v[2], p.beta * old.z);
-            out.w = fmaf(p.alpha, v[3], p.beta * old.w);
-          } else {
-            out = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2],
-                              p.alpha * v[3]);
-          }
-          *reinterpret_cast<float4 *>(dst) = out;
-        } else {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (col + e < p.N) {
-              dst[e] = (p.beta != 0.0f) ? fmaf(p.alpha, v[e], p.beta * dst[e])
-                                        : p.alpha * v[e];
-            }
+        for (int e = 0; e < 4; ++e) {
+          if (col + e < p.N) {
+            dst[e] = (p.beta != 0.0f) ? fmaf(p.alpha, v[e], p.beta * dst[e]) : p.alpha * v[e];
           }
         }
       }

@@ -18,37 +18,48 @@ struct Problem {
 
 // Shape of one compiled tile configuration (mirrors TileConfig in sgemm_ffma.cuh).
 struct VariantShape {
-  int BM, BN, BK, threads, TM, TN, stages, min_blocks, smem_bytes;
+  int BM, BN, BK, threads, TM, TN, stages, min_blocks, mode, smem_bytes;
   double eff;  // modelled fraction of the FP32 pipe this configuration sustains
+  bool automatic;  // considered by the automatic plan (others only when forced)
 };
 
-constexpr int smem_of(int BM, int BN, int BK, int stages) {
-  return stages * BK * (BM + BN) * 4;
+// mode: 0 scalar FFMA, 1 FFMA2 with register broadcast, 2 FFMA2 with duplicated A in smem
+constexpr int smem_of(int BM, int BN, int BK, int stages, int mode) {
+  return stages * BK * (BM * (mode == 2 ? 2 : 1) + BN) * 4;
 }
 
 constexpr VariantShape kVariants[] = {
-    {128, 256, 16, 256, 16, 8, 3, 1, smem_of(128, 256, 16, 3), 1.00},
-    {128, 128, 16, 256, 8, 8, 4, 2, smem_of(128, 128, 16, 4), 0.90},
-    {64, 64, 16, 128, 8, 4, 4, 4, smem_of(64, 64, 16, 4), 0.70},
-    {16, 256, 32, 128, 8, 4, 3, 2, smem_of(16, 256, 32, 3), 0.60},
-    {256, 16, 32, 128, 8, 4, 3, 2, smem_of(256, 16, 32, 3), 0.60},
+    {128, 256, 16, 256, 16, 8, 3, 1, 0, smem_of(128, 256, 16, 3, 0), 0.78, true},
+    {128, 128, 16, 256, 8, 8, 4, 2, 0, smem_of(128, 128, 16, 4, 0), 0.72, true},
+    {64, 64, 16, 128, 8, 4, 4, 4, 0, smem_of(64, 64, 16, 4, 0), 0.60, true},
+    {16, 256, 32, 128, 8, 4, 3, 2, 0, smem_of(16, 256, 32, 3, 0), 0.50, true},
+    {256, 16, 32, 128, 8, 4, 3, 2, 0, smem_of(256, 16, 32, 3, 0), 0.50, true},
+    {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.86, true},
+    {128, 256, 16, 256, 8, 16, 3, 1, 2, smem_of(128, 256, 16, 3, 2), 0.80, false},
+    {128, 256, 32, 256, 8, 16, 3, 1, 2, smem_of(128, 256, 32, 3, 2), 0.80, false},
+    {128, 128, 16, 256, 8, 8, 4, 2, 1, smem_of(128, 128, 16, 4, 1), 0.83, true},
+    {128, 256, 16, 512, 8, 8, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false},
+    {256, 128, 16, 512, 8, 8, 3, 1, 1, smem_of(256, 128, 16, 3, 1), 0.80, false},
+    {128, 256, 32, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 32, 3, 1), 0.80, false},
+    {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false},
+    {128, 256, 16, 256, 8, 16, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.88, true},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
 struct Plan {
   int variant = -1;     // -1: no GEMM kernel (beta-scale only, or nothing)
-  int split = 1;        // K slices
+  int main_tiles = 0;   // tiles computed whole by CTAs 0 .. main_tiles-1
+  int split = 1;        // K slices of each remaining tile (1: no split-K)
   int k_per_split = 0;  // K elements per slice (multiple of BK)
   int tiles_m = 0, tiles_n = 0;
   int group_m = 1;
+  int ctas = 0;         // GEMM grid size
   int launches = 0;
   size_t ws_bytes = 0;
+  double cycles = 0;    // modelled cost
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
-
-// Row stride of split-K partials: N rounded up to 4 so every row starts 16-byte aligned.
-inline long long workspace_ld(int N) { return ceil_div(N, 4) * 4; }
 
 // BLAS-style check: the first illegal argument, numbered from 1 in the sgemm_f32 order
 // (M, N, K, alpha, A, lda, B, ldb, beta, C, ldc). A and B only have to be present when
@@ -68,81 +79,121 @@ inline int validate(const Problem &p, float alpha, bool hasA, bool hasB, bool ha
   return 0;
 }
 
-// Modelled cost, in SM cycles, of running variant v with `split` K slices.
-// GEMM kernel: the busiest SM runs ceil(ctas / SMs) CTAs, each BM*BN*k_slice FMAs at
-// 128 FMA/cycle scaled by the variant's efficiency, plus ~2500 cycles of pipeline fill and
-// epilogue; it overlaps with streaming the algorithmic bytes (and the split-K partials it
-// writes) at ~3400 bytes/cycle for the chip. Split-K adds a reduction kernel that runs
-// after it: partials read, C read (beta != 0) and written, plus ~2000 cycles of launch.
-inline double model_cycles(const Problem &p, int v, int split, int num_sms, bool beta_nz,
-                           int *k_per_split_out, int *split_eff_out) {
+// Modelled cost, in SM cycles, of variant v with `main` whole tiles and the rest split
+// into `split` K slices. `slots` CTAs run at once (SMs x CTAs per SM), each at 1/min_blocks
+// of its SM's 128 FMA/cycle scaled by the variant's efficiency, plus ~2500 cycles of
+// pipeline fill and epilogue per CTA. Whole tiles run first (CTA order), then the slices.
+// The GEMM overlaps with streaming its algorithmic bytes at ~3400 bytes/cycle for the
+// chip. Split tiles add a reduction kernel afterwards: partials read, C read (beta != 0)
+// and written, plus ~2000 cycles of launch.
+inline Plan model_plan(const Problem &p, int v, long long main, int split, int num_sms,
+                       bool beta_nz) {
   const VariantShape &s = kVariants[v];
-  const long long tiles = ceil_div(p.M, s.BM) * ceil_div(p.N, s.BN);
+  Plan pl;
+  pl.variant = v;
+  pl.tiles_m = (int)ceil_div(p.M, s.BM);
+  pl.tiles_n = (int)ceil_div(p.N, s.BN);
+  const long long tiles = (long long)pl.tiles_m * pl.tiles_n;
   const long long kt = ceil_div(p.K, s.BK);
+  if (split <= 1 || main >= tiles) {
+    split = 1;
+    main = tiles;
+  }
   const long long kt_per = ceil_div(kt, split);
-  const long long split_eff = ceil_div(kt, kt_per);
-  const long long ctas = tiles * split_eff;
-  const double per_sm = (double)ceil_div(ctas, num_sms);
-  const double fmas = (double)s.BM * s.BN * (double)(kt_per * s.BK);
-  const double compute = per_sm * (fmas / (128.0 * s.eff) + 2500.0);
-  const double mn = (double)p.M * (double)workspace_ld(p.N);
+  split = (int)ceil_div(kt, kt_per);  // no empty slices
+  if (split == 1) main = tiles;
+  const long long tail = tiles - main;
+  const long long slots = (long long)num_sms * s.min_blocks;
+  const double rate = 128.0 * s.eff / s.min_blocks;  // FMA per cycle per resident CTA
+  const double t_full = (double)s.BM * s.BN * (double)(kt * s.BK) / rate + 2500.0;
+  const double t_slice = (double)s.BM * s.BN * (double)(kt_per * s.BK) / rate + 2500.0;
+  double compute = (double)(main / slots) * t_full;
+  const long long rem_full = main % slots;  // shares a wave with the first slices
+  const long long slices = tail * split;
+  if (rem_full > 0 || slices > 0) {
+    const double mix = (double)rem_full * t_full + (double)slices * t_slice;
+    const double wave = std::max(rem_full > 0 ? t_full : 0.0, slices > 0 ? t_slice : 0.0);
+    compute += std::max(wave, mix / (double)slots);
+  }
+  const double mn_c = (double)p.M * p.N * 4.0 * (beta_nz ? 2.0 : 1.0);
   double gemm_bytes = 4.0 * ((double)p.M * p.K + (double)p.K * p.N);
   double reduce = 0.0;
-  if (split_eff > 1) {
-    gemm_bytes += 4.0 * split_eff * mn;
-    reduce = 4.0 * (split_eff + (beta_nz ? 2.0 : 1.0)) * mn / 3400.0 + 2000.0;
+  const double part_bytes = (double)slices * s.BM * s.BN * 4.0;
+  if (slices > 0) {
+    const double tail_frac = (double)tail / (double)tiles;
+    gemm_bytes += part_bytes + mn_c * (1.0 - tail_frac);
+    reduce = (part_bytes + mn_c * tail_frac) / 3400.0 + 2000.0;
   } else {
-    gemm_bytes += 4.0 * mn * (beta_nz ? 2.0 : 1.0);
+    gemm_bytes += mn_c;
   }
-  if (k_per_split_out) *k_per_split_out = (int)(kt_per * s.BK);
-  if (split_eff_out) *split_eff_out = (int)split_eff;
-  return std::max(compute, gemm_bytes / 3400.0) + reduce;
+  pl.main_tiles = (int)main;
+  pl.split = split;
+  pl.k_per_split = (int)(kt_per * s.BK);
+  pl.group_m = std::min(8, pl.tiles_m);
+  pl.ctas = (int)(main + slices);
+  pl.launches = slices > 0 ? 2 : 1;
+  pl.ws_bytes = slices > 0 ? (size_t)part_bytes : 0;
+  pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce;
+  if (main + slices > 0x7fffffffLL) {  // grid too large for one launch
+    pl.ctas = 0;
+    pl.cycles = std::numeric_limits<double>::infinity();
+  }
+  return pl;
 }
 
-// Choose the tile configuration and split-K factor. force_v >= 0 pins the variant;
-// force_split >= 1 pins the split (clamped to the number of K tiles).
+// Choose the tile configuration and the split-K layout. Candidates per variant: no split;
+// every tile split in s slices; and, when the tiles do not fill the last wave, the full
+// waves whole with only the last wave's tiles split (s chosen to fill that wave).
+// force_v >= 0 pins the variant. force_split >= 1 splits every tile into that many slices
+// (1: none); force_split == -1 takes the whole-waves-plus-split-tail layout with the
+// automatic slice count, force_split <= -2 the same layout with -force_split slices;
+// 0 leaves the choice to the model.
 inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, int force_v,
                       int force_split) {
-  Plan pl;
-  if (p.M == 0 || p.N == 0) return pl;
+  Plan best;
+  if (p.M == 0 || p.N == 0) return best;  // nothing to launch
   if (alpha == 0.0f || p.K == 0) {
-    pl.launches = (beta == 1.0f) ? 0 : 1;
-    return pl;
+    best.launches = (beta == 1.0f) ? 0 : 1;
+    return best;
   }
   num_sms = std::max(1, num_sms);
   const bool beta_nz = beta != 0.0f;
-  double best = std::numeric_limits<double>::infinity();
-  int best_v = 0, best_split = 1, best_kps = 0;
+  best.cycles = std::numeric_limits<double>::infinity();
+  const double ws_cap = 512.0 * 1024 * 1024;
+  auto consider = [&](const Plan &c) {
+    if ((double)c.ws_bytes > ws_cap && force_split < 1) return;
+    if (c.cycles < best.cycles * 0.999) best = c;  // prefer earlier (simpler) on ties
+  };
   const int v_lo = force_v >= 0 ? force_v : 0;
   const int v_hi = force_v >= 0 ? force_v : kNumVariants - 1;
   for (int v = v_lo; v <= v_hi; ++v) {
-    const long long kt = ceil_div(p.K, kVariants[v].BK);
+    if (force_v < 0 && !kVariants[v].automatic) continue;
+    const VariantShape &s = kVariants[v];
+    const long long tiles = ceil_div(p.M, s.BM) * ceil_div(p.N, s.BN);
+    const long long kt = ceil_div(p.K, s.BK);
     const int max_split = (int)std::min<long long>(64, kt);
-    const int s_lo = force_split >= 1 ? std::min(force_split, max_split) : 1;
-    const int s_hi = force_split >= 1 ? s_lo : max_split;
-    for (int sp = s_lo; sp <= s_hi; ++sp) {
-      int kps = 0, seff = 0;
-      const double c = model_cycles(p, v, sp, num_sms, beta_nz, &kps, &seff);
-      const double ws = seff > 1 ? 4.0 * seff * (double)p.M * (double)workspace_ld(p.N) : 0;
-      if (force_split < 1 && ws > 512.0 * 1024 * 1024) continue;  // workspace cap
-      if (c < best * 0.999) {  // prefer fewer slices on (near) ties
-        best = c;
-        best_v = v;
-        best_split = seff;
-        best_kps = kps;
-      }
+    if (force_split >= 1) {
+      consider(model_plan(p, v, 0, std::min(force_split, max_split), num_sms, beta_nz));
+      continue;
+    }
+    const long long slots = (long long)num_sms * s.min_blocks;
+    const long long main = (tiles / slots) * slots;
+    const long long tail = tiles - main;
+    if (force_split <= -1) {
+      int sp = force_split == -1 ? (int)std::max<long long>(2, tail ? slots / tail : 2)
+                                 : -force_split;
+      sp = std::min(sp, max_split);
+      consider(model_plan(p, v, tail > 0 ? main : tiles, sp, num_sms, beta_nz));
+      continue;
+    }
+    consider(model_plan(p, v, tiles, 1, num_sms, beta_nz));
+    for (int sp = 2; sp <= max_split; ++sp) consider(model_plan(p, v, 0, sp, num_sms, beta_nz));
+    if (main > 0 && tail > 0) {
+      const int sp = (int)std::min<long long>(max_split, std::max<long long>(2, slots / tail));
+      consider(model_plan(p, v, main, sp, num_sms, beta_nz));
     }
   }
-  const VariantShape &s = kVariants[best_v];
-  pl.variant = best_v;
-  pl.split = best_split;
-  pl.k_per_split = best_split > 1 ? best_kps : (int)(ceil_div(p.K, s.BK) * s.BK);
-  pl.tiles_m = (int)ceil_div(p.M, s.BM);
-  pl.tiles_n = (int)ceil_div(p.N, s.BN);
-  pl.group_m = std::min(8, pl.tiles_m);
-  pl.launches = best_split > 1 ? 2 : 1;
-  pl.ws_bytes = best_split > 1 ? (size_t)4 * best_split * (size_t)p.M * workspace_ld(p.N) : 0;
-  return pl;
+  return best;
 }
 
 }  // namespace sgemm

@@ -96,12 +96,15 @@ int sgemm_f32_ws(int M, int N, int K, float alpha, const float *A, int lda, cons
  * Outputs (any may be NULL):
  *   variant  tile configuration index (0 .. sgemm_f32_num_variants() - 1), -1 when no
  *            GEMM kernel runs (empty problem or beta-scale only)
- *   split    number of K slices (1 = no split-K)
- *   launches kernels enqueued by one sgemm_f32 call
- *   ws_bytes split-K workspace bytes
+ *   split      K slices of each split tile (1 = no split-K)
+ *   main_tiles tiles computed whole; the remaining tiles are split into `split` K slices
+ *              and finished by a second, reducing kernel
+ *   launches   kernels enqueued by one sgemm_f32 call
+ *   ws_bytes   split-K workspace bytes
  * Returns the same negative codes as sgemm_f32 for illegal arguments, else 0. */
 int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta,
-                   int num_sms, int *variant, int *split, int *launches, size_t *ws_bytes);
+                   int num_sms, int *variant, int *split, int *main_tiles, int *launches,
+                   size_t *ws_bytes);
 
 /* Tile configurations compiled into the library, for tests and tuning. */
 int sgemm_f32_num_variants(void);
@@ -111,10 +114,13 @@ int sgemm_f32_num_variants(void);
 int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *TM,
                            int *TN, int *stages);
 
-/* sgemm_f32 with the plan forced: `variant` in [0, sgemm_f32_num_variants()) and
- * `split` >= 1 (clamped so that every slice holds at least one K tile). Pass variant = -1
- * and split = 0 for the automatic plan. For tests and tuning sweeps; results satisfy the
- * same contract as sgemm_f32. Returns -14 for an out-of-range variant. */
+/* sgemm_f32 with the plan forced, for tests and tuning sweeps; results satisfy the same
+ * contract as sgemm_f32. `variant` in [0, sgemm_f32_num_variants()) pins the tile
+ * configuration (-1: automatic). `split` >= 1 splits every tile into that many K slices
+ * (1: no split-K); -1 computes the full waves of tiles whole and splits only the tiles of
+ * the last, partial wave (slice count chosen to fill it); <= -2 does the same with
+ * -split slices; 0 is automatic. Slice counts are clamped so that every slice holds at
+ * least one K tile. Returns -14 for an out-of-range variant. */
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);

@@ -110,13 +110,27 @@ def test_plan_thin_shapes_use_thin_tiles_and_split_k():
 
 
 def test_plan_workspace_formula():
-    for shp in [(16, 4096, 4096), (4096, 16, 8192), (256, 256, 256), (1023, 1021, 4096)]:
+    """Workspace = one BM x BN float tile per K slice of every split tile."""
+    for shp in [(16, 4096, 4096), (4096, 16, 8192), (256, 256, 256), (1023, 1021, 4096),
+                (8192, 8192, 8192), (4097, 4097, 4097)]:
         M, N, K = shp
         p = _plan(M, N, K)
+        info = sg.sgemm_f32_variant_info(p["variant"])
+        tiles = -(-M // info["BM"]) * -(-N // info["BN"])
+        split_tiles = tiles - p["main_tiles"]
         if p["split"] > 1:
-            assert p["ws_bytes"] == 4 * p["split"] * M * ((N + 3) // 4 * 4)
+            assert split_tiles > 0 and p["launches"] == 2
+            assert p["ws_bytes"] == 4 * p["split"] * split_tiles * info["BM"] * info["BN"]
         else:
-            assert p["ws_bytes"] == 0
+            assert p["main_tiles"] == tiles and p["ws_bytes"] == 0 and p["launches"] == 1
+
+
+def test_plan_tail_split_keeps_whole_waves():
+    """When the tiles overflow the last wave, whole waves stay unsplit."""
+    p = _plan(8192, 8192, 8192)
+    if p["split"] > 1 and p["main_tiles"] > 0:
+        info = sg.sgemm_f32_variant_info(p["variant"])
+        assert p["main_tiles"] % SMS == 0
 
 
 def test_plan_split_never_exceeds_k_tiles():

@@ -15,6 +15,7 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
+NUM_VARIANTS = 14  # compiled tile configurations; checked against the library below
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -100,8 +101,8 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
           (255, 31, 100), (16, 300, 257), (300, 16, 129), (257, 255, 1)]
 
 
-@pytest.mark.parametrize("variant", range(5))
-@pytest.mark.parametrize("split", [1, 3])
+@pytest.mark.parametrize("variant", range(NUM_VARIANTS))
+@pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
     for (M, N, K) in RAGGED:
@@ -115,6 +116,19 @@ def test_variant_ragged(variant, split, aligned):
         assert guard, (M, N, K)
         R, S = oracle.sgemm_f64(A, B, C, 0.75, -1.25)
         assert_bound(out.numpy(), R, S, -1.25, C.numpy(), f"v{variant} s{split} {M,N,K}")
+
+
+@pytest.mark.parametrize("variant", [0, 5, 8])
+@pytest.mark.parametrize("split", [-1, -3])
+def test_whole_waves_plus_split_tail(variant, split):
+    """More tiles than fit in one wave: the full waves run whole, the tiles of the last
+    wave are split along K and finished by the reduce kernel."""
+    M, N, K = 2100, 2600, 300  # 17 x 11 = 187 tiles of 128 x 256; 289 of 128 x 128
+    A, B, C = make_inputs(M, N, K, seed=77)
+    out, guard = _run(A, B, C, 1.5, 0.5, variant=variant, split=split)
+    assert guard
+    R, S = oracle.sgemm_f64(A, B, C, 1.5, 0.5)
+    assert_bound(out.numpy(), R, S, 0.5, C.numpy(), f"v{variant} tail split {split}")
 
 
 def test_ragged_sweep_auto_plan():
@@ -132,6 +146,10 @@ def test_ragged_sweep_auto_plan():
 
 # --------------------------------------------------------------------------------------
 # BLAS special cases and contract details.
+
+def test_variant_count():
+    assert sg.sgemm_f32_num_variants() == NUM_VARIANTS
+
 
 def test_beta_zero_does_not_read_c():
     A, B, _ = make_inputs(70, 90, 33, seed=5)
