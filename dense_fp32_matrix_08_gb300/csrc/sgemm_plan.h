@@ -82,7 +82,8 @@ inline int validate(const Problem &p, float alpha, bool hasA, bool hasB, bool ha
 // Modelled cost, in SM cycles, of variant v with `main` whole tiles and the rest split
 // into `split` K slices. `slots` CTAs run at once (SMs x CTAs per SM), each at 1/min_blocks
 // of its SM's 128 FMA/cycle scaled by the variant's efficiency, plus ~2500 cycles of
-// pipeline fill and epilogue per CTA. Whole tiles run first (CTA order), then the slices.
+// pipeline fill and epilogue per CTA; a slice also stores its BM x BN partial tile at the
+// SM's share of the chip's bandwidth. Whole tiles run first (CTA order), then the slices.
 // The GEMM overlaps with streaming its algorithmic bytes at ~3400 bytes/cycle for the
 // chip. Split tiles add a reduction kernel afterwards: partials read, C read (beta != 0)
 // and written, plus ~2000 cycles of launch.
@@ -106,7 +107,8 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   const long long slots = (long long)num_sms * s.min_blocks;
   const double rate = 128.0 * s.eff / s.min_blocks;  // FMA per cycle per resident CTA
   const double t_full = (double)s.BM * s.BN * (double)(kt * s.BK) / rate + 2500.0;
-  const double t_slice = (double)s.BM * s.BN * (double)(kt_per * s.BK) / rate + 2500.0;
+  const double t_slice = (double)s.BM * s.BN * (double)(kt_per * s.BK) / rate + 2500.0 +
+                         (double)s.BM * s.BN * 4.0 / (3400.0 / num_sms);
   double compute = (double)(main / slots) * t_full;
   const long long rem_full = main % slots;  // shares a wave with the first slices
   const long long slices = tail * split;
@@ -159,7 +161,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   num_sms = std::max(1, num_sms);
   const bool beta_nz = beta != 0.0f;
   best.cycles = std::numeric_limits<double>::infinity();
-  const double ws_cap = 512.0 * 1024 * 1024;
+  const double ws_cap = 64.0 * 1024 * 1024;  // largest split-K workspace the plan may use
   auto consider = [&](const Plan &c) {
     if ((double)c.ws_bytes > ws_cap && force_split < 1) return;
     if (c.cycles < best.cycles * 0.999) best = c;  // prefer earlier (simpler) on ties
