@@ -18,13 +18,13 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "LIB_PATH", "SgemmError", "lib", "sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced",
     "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
-    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm", "EXPORTED",
+    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
 EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspace_size",
             "sgemm_f32_plan", "sgemm_f32_num_variants", "sgemm_f32_variant_info",
-            "sgemm_f32_version")
+            "sgemm_f32_version", "sgemm_f32_noalloc")
 
 
 class SgemmError(RuntimeError):
@@ -48,6 +48,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32.argtypes = gemm + [vp]
     L.sgemm_f32_ws.argtypes = gemm + [vp, sz, vp]
     L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
+    L.sgemm_f32_noalloc.argtypes = gemm + [vp]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
@@ -103,6 +104,14 @@ def sgemm_f32_forced(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant, spli
                      stream=None) -> int:
     return lib.sgemm_f32_forced(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
                                 ldc, variant, split, _stream(stream))
+
+
+def sgemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """sgemm_f32 for callers that may not allocate device memory: any split-K workspace
+    comes from the library's fixed per-device scratch array (see include/sgemm_f32.h).
+    Returns the C status; -15 means the problem needs more scratch than that array."""
+    return lib.sgemm_f32_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
+                                 ldc, _stream(stream))
 
 
 def sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc) -> tuple[int, int]:

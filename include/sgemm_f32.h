@@ -58,6 +58,8 @@
  *   -10  C == NULL while M > 0 and N > 0
  *   -11  ldc < max(1, N)
  *   -13  (sgemm_f32_ws only) workspace too small or NULL while one is needed
+ *   -15  (sgemm_f32_noalloc only) the problem needs more split-K scratch than the
+ *        library's fixed array holds
  *   >0   a cudaError_t from a launch or a stream-ordered allocation
  *   Nothing is launched when an argument is illegal. The library never aborts or traps.
  */
@@ -124,6 +126,44 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);
+
+/* Size of the fixed device scratch array used by sgemm_f32_noalloc, and its error code. */
+#define SGEMM_F32_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB per device */
+#define SGEMM_F32_ERR_SCRATCH_TOO_SMALL (-15)
+
+/* C = alpha * A * B + beta * C exactly like sgemm_f32 (same plan, same kernels, bitwise the
+ * same result), for callers that are not allowed to allocate device memory. The source
+ * pages have no counterpart of this entry point; it exists for how the library is used.
+ *
+ * Who needs it: code running inside a host framework that owns all device memory and does
+ * not let libraries allocate (for example a plugin of an inference runtime whose memory is
+ * planned up front), and real-time or certified loops that forbid allocation after start-up.
+ * For them cudaMalloc and cudaMallocAsync are off limits: an allocation can block or
+ * synchronise, can fail under memory pressure at any point, and bypasses the caller's own
+ * accounting of device memory.
+ *
+ * How: the split-K workspace that sgemm_f32 takes from cudaMallocAsync comes instead from a
+ * fixed array of SGEMM_F32_NOALLOC_SCRATCH_BYTES in device global memory owned by the
+ * library; every GPU that loads the library holds that array until the process exits. The
+ * call makes no cudaMalloc, cudaMallocAsync, cudaFree or other allocating call. The caller
+ * still passes A, B and C, as for sgemm_f32.
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current. Make that first call on a device before
+ * any stream capture on it.
+ *
+ * Sharing: all calls in the process share the one array of a device, which keeps whatever
+ * the last call left in it. Calls ordered on the GPU (the same stream, or streams ordered by
+ * events) are safe. Calls that can overlap on the GPU (unordered streams, for example from
+ * several host threads) race on the array and give wrong results. Nothing in the array has
+ * to start at zero: a call writes every workspace element before it reads it.
+ *
+ * Errors: as sgemm_f32, plus SGEMM_F32_ERR_SCRATCH_TOO_SMALL when the problem's split-K
+ * plan needs more workspace than the array holds (sgemm_f32_workspace_size() reports the
+ * need beforehand); nothing is launched in that case. */
+int sgemm_f32_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
+                      const float *B, int ldb, float beta, float *C, int ldc,
+                      cudaStream_t stream);
 
 /* Library version string, e.g. "sgemm_f32 0.1.0 sm_103a". */
 const char *sgemm_f32_version(void);
