@@ -207,8 +207,15 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
   const int warp = tid >> 5;
   const int warp_m = warp / Cfg::WARPS_N;
   const int warp_n = warp % Cfg::WARPS_N;
-  const int lane_m = lane / LN;
-  const int lane_n = lane % LN;
+  // Lane layout inside the warp tile. Shared-memory loads merge equal addresses only
+  // within aligned groups of 4 lanes, and a 128-bit load costs max(2, distinct addresses
+  // per 4-lane group) wavefronts (measured on sm_103a). Each 4-lane group is therefore a
+  // 2 x 2 block of (lane_m, lane_n): both the A and the B fragment loads then take the
+  // 2-wavefront minimum (a row-major lane order would cost 4 for one of them).
+  static_assert(LM >= 2 && LN >= 2, "2 x 2 lane groups need LM, LN >= 2");
+  const int lane_hi = lane >> 2;
+  const int lane_n = (lane_hi % (LN / 2)) * 2 + (lane & 1);
+  const int lane_m = (lane_hi / (LN / 2)) * 2 + ((lane >> 1) & 1);
 
   // which tile, which K range (see GemmParams)
   const int w = blockIdx.x;

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <algorithm>
+#include <cmath>
 #include <cstddef>
 #include <cstdint>
 #include <limits>
@@ -43,6 +44,12 @@ constexpr VariantShape kVariants[] = {
     {128, 256, 32, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 32, 3, 1), 0.80, false},
     {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false},
     {128, 256, 16, 256, 8, 16, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.88, true},
+    {128, 64, 16, 128, 8, 8, 3, 2, 1, smem_of(128, 64, 16, 3, 1), 0.80, false},
+    {128, 64, 16, 128, 8, 8, 4, 2, 1, smem_of(128, 64, 16, 4, 1), 0.80, false},
+    {128, 128, 16, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.90, true},
+    {128, 64, 16, 128, 8, 8, 3, 3, 1, smem_of(128, 64, 16, 3, 1), 0.80, false},
+    {128, 256, 16, 256, 4, 32, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.80, false},
+    {128, 128, 16, 128, 4, 32, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.80, false},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -109,13 +116,22 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   const double t_full = (double)s.BM * s.BN * (double)(kt * s.BK) / rate + 2500.0;
   const double t_slice = (double)s.BM * s.BN * (double)(kt_per * s.BK) / rate + 2500.0 +
                          (double)s.BM * s.BN * 4.0 / (3400.0 / num_sms);
-  double compute = (double)(main / slots) * t_full;
-  const long long rem_full = main % slots;  // shares a wave with the first slices
+  // CTAs start in index order, `slots` at a time: whole tiles first, then slices. A round
+  // with fewer CTAs than slots leaves some SMs with fewer resident CTAs, which then run
+  // faster, nearly in proportion: a CTA alone on an SM that holds min_blocks takes about
+  // (1 / min_blocks)^0.85 of its shared-SM time (calibrated on 4096^3 and 8192^3).
   const long long slices = tail * split;
-  if (rem_full > 0 || slices > 0) {
-    const double mix = (double)rem_full * t_full + (double)slices * t_slice;
-    const double wave = std::max(rem_full > 0 ? t_full : 0.0, slices > 0 ? t_slice : 0.0);
-    compute += std::max(wave, mix / (double)slots);
+  const long long total = main + slices;
+  double compute = 0.0;
+  for (long long first = 0; first < total;) {
+    const long long n = std::min(slots, total - first);
+    const long long full_in = std::max(0LL, std::min(main, first + n) - first);
+    const double t = full_in > 0 ? t_full : t_slice;
+    const long long per_sm = ceil_div(n, num_sms);
+    compute += t * std::pow((double)per_sm / s.min_blocks, 0.85);
+    const long long rounds_same = (full_in == n && n == slots) ? (main - first) / slots : 1;
+    compute += t * (double)(std::max(1LL, rounds_same) - 1);
+    first += n * std::max(1LL, rounds_same);
   }
   const double mn_c = (double)p.M * p.N * 4.0 * (beta_nz ? 2.0 : 1.0);
   double gemm_bytes = 4.0 * ((double)p.M * p.K + (double)p.K * p.N);
@@ -131,7 +147,7 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   pl.main_tiles = (int)main;
   pl.split = split;
   pl.k_per_split = (int)(kt_per * s.BK);
-  pl.group_m = std::min(8, pl.tiles_m);
+  pl.group_m = std::min(16, pl.tiles_m);
   pl.ctas = (int)(main + slices);
   pl.launches = slices > 0 ? 2 : 1;
   pl.ws_bytes = slices > 0 ? (size_t)part_bytes : 0;
@@ -190,7 +206,9 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
     }
     consider(model_plan(p, v, tiles, 1, num_sms, beta_nz));
     for (int sp = 2; sp <= max_split; ++sp) consider(model_plan(p, v, 0, sp, num_sms, beta_nz));
-    if (main > 0 && tail > 0) {
+    // Split tails only for one-CTA-per-SM configurations: with several CTAs per SM a
+    // partial last wave already runs with fewer CTAs per SM, each of them faster.
+    if (main > 0 && tail > 0 && s.min_blocks == 1) {
       const int sp = (int)std::min<long long>(max_split, std::max<long long>(2, slots / tail));
       consider(model_plan(p, v, main, sp, num_sms, beta_nz));
     }

@@ -35,9 +35,16 @@ template <> struct VariantCfg<10> { using type = TileConfig<256, 128, 16, 64, 32
 template <> struct VariantCfg<11> { using type = TileConfig<128, 256, 32, 64, 64, 8, 16, 3, 1, 1>; };
 template <> struct VariantCfg<12> { using type = TileConfig<128, 256, 16, 32, 128, 8, 16, 3, 1, 1>; };
 template <> struct VariantCfg<13> { using type = TileConfig<128, 256, 16, 64, 64, 8, 16, 4, 1, 1>; };
+template <> struct VariantCfg<14> { using type = TileConfig<128, 64, 16, 64, 32, 8, 8, 3, 2, 1>; };
+template <> struct VariantCfg<15> { using type = TileConfig<128, 64, 16, 64, 32, 8, 8, 4, 2, 1>; };
+template <> struct VariantCfg<16> { using type = TileConfig<128, 128, 16, 64, 64, 8, 16, 3, 2, 1>; };
+template <> struct VariantCfg<17> { using type = TileConfig<128, 64, 16, 64, 32, 8, 8, 3, 3, 1>; };
+template <> struct VariantCfg<18> { using type = TileConfig<128, 256, 16, 32, 128, 4, 32, 4, 1, 1>; };
+template <> struct VariantCfg<19> { using type = TileConfig<128, 128, 16, 32, 128, 4, 32, 3, 2, 1>; };
 
 #define SGEMM_FOR_EACH_VARIANT(X) \
-  X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13)
+  X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) \
+  X(16) X(17) X(18) X(19)
 
 template <class Cfg>
 constexpr bool matches(const VariantShape &s) {
