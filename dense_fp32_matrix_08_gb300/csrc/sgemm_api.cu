@@ -29,6 +29,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   std::once_flag once;
   int num_sms = 0;
+  cudaMemPool_t pool = nullptr;  // split-K workspace pool of this device
   cudaError_t err = cudaSuccess;
 };
 static DeviceState g_dev[kMaxDevices];
@@ -46,11 +47,62 @@ static cudaError_t device_setup(int *num_sms) {
       for (int a = 0; a < 2 && err == cudaSuccess; ++a)
         err = cudaFuncSetAttribute(kKernels[v].k[a], cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    kKernels[v].smem);
+    // A pool of the library's own for split-K workspaces. It keeps freed memory (release
+    // threshold: never), so a stream-ordered allocation of a recently freed size is a
+    // cheap reuse instead of a fresh mapping; the default pool returns its memory at every
+    // synchronisation. The pool holds at most the largest workspace the planner chooses
+    // (64 MiB) plus whatever concurrent calls on several streams need at once.
+    if (err == cudaSuccess) {
+      cudaMemPoolProps props = {};
+      props.allocType = cudaMemAllocationTypePinned;
+      props.location.type = cudaMemLocationTypeDevice;
+      props.location.id = dev;
+      err = cudaMemPoolCreate(&st.pool, &props);
+      if (err == cudaSuccess) {
+        uint64_t keep = ~0ull;
+        err = cudaMemPoolSetAttribute(st.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+      }
+    }
     st.num_sms = sms;
     st.err = err;
   });
   *num_sms = st.num_sms;
   return st.err;
+}
+
+// make_plan evaluates a few hundred candidate layouts; a small per-thread cache keeps
+// repeated calls on the same shape at a table lookup. The plan depends only on the shape,
+// the special values of alpha and beta, the SM count and the forcing arguments.
+static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms, int force_v,
+                        int force_split) {
+  struct Entry {
+    int M, N, K, num_sms, force_v, force_split;
+    unsigned flags;
+    bool valid;
+    Plan plan;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  const unsigned flags = (alpha == 0.0f ? 1u : 0u) | (beta != 0.0f ? 2u : 0u) |
+                         (beta == 1.0f ? 4u : 0u);
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry &e = cache[i];
+    if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
+        e.force_v == force_v && e.force_split == force_split && e.flags == flags)
+      return e.plan;
+  }
+  Entry &e = cache[next];
+  next = (next + 1) % kEntries;
+  e = Entry{pr.M, pr.N, pr.K, num_sms, force_v, force_split, flags, true,
+            make_plan(pr, alpha, beta, num_sms, force_v, force_split)};
+  return e.plan;
+}
+
+static cudaMemPool_t workspace_pool() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_dev[dev].pool;
 }
 
 static inline bool aligned16(const void *p) {
@@ -126,14 +178,15 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
-  Plan pl = make_plan(pr, alpha, beta, num_sms, force_v, force_split);
+  Plan pl = cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
   float *wsp = nullptr;
   if (pl.ws_bytes > 0) {
     if (ws_mode == 1) {
       if (ws == nullptr || ws_bytes < pl.ws_bytes || !aligned16(ws)) return kErrWorkspace;
       wsp = static_cast<float *>(ws);
     } else {
-      e = cudaMallocAsync(reinterpret_cast<void **>(&wsp), pl.ws_bytes, stream);
+      e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(&wsp), pl.ws_bytes,
+                                  workspace_pool(), stream);
       if (e != cudaSuccess) return (int)e;
     }
   }
@@ -191,7 +244,7 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
   if (M == 0 || N == 0) {
     pl.variant = -1;
   } else {
-    pl = make_plan(pr, alpha, beta, num_sms, -1, 0);
+    pl = cached_plan(pr, alpha, beta, num_sms, -1, 0);
   }
   if (variant) *variant = pl.variant;
   if (split) *split = pl.split;

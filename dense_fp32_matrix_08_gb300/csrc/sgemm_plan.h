@@ -120,19 +120,23 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   // with fewer CTAs than slots leaves some SMs with fewer resident CTAs, which then run
   // faster, nearly in proportion: a CTA alone on an SM that holds min_blocks takes about
   // (1 / min_blocks)^0.85 of its shared-SM time (calibrated on 4096^3 and 8192^3).
+  // Closed form (no loop over rounds): full rounds of whole tiles; one round mixing the
+  // remaining whole tiles with the first slices; full rounds of slices; a last partial
+  // round of slices.
   const long long slices = tail * split;
-  const long long total = main + slices;
-  double compute = 0.0;
-  for (long long first = 0; first < total;) {
-    const long long n = std::min(slots, total - first);
-    const long long full_in = std::max(0LL, std::min(main, first + n) - first);
-    const double t = full_in > 0 ? t_full : t_slice;
-    const long long per_sm = ceil_div(n, num_sms);
-    compute += t * std::pow((double)per_sm / s.min_blocks, 0.85);
-    const long long rounds_same = (full_in == n && n == slots) ? (main - first) / slots : 1;
-    compute += t * (double)(std::max(1LL, rounds_same) - 1);
-    first += n * std::max(1LL, rounds_same);
+  auto partial = [&](long long n, double t) {
+    return n > 0 ? t * std::pow((double)ceil_div(n, num_sms) / s.min_blocks, 0.85) : 0.0;
+  };
+  double compute = (double)(main / slots) * t_full;
+  const long long rem_full = main % slots;
+  long long rem_slices = slices;
+  if (rem_full > 0) {
+    const long long mixed = std::min(slots - rem_full, rem_slices);
+    rem_slices -= mixed;
+    compute += partial(rem_full + mixed, t_full);
   }
+  compute += (double)(rem_slices / slots) * t_slice;
+  compute += partial(rem_slices % slots, t_slice);
   const double mn_c = (double)p.M * p.N * 4.0 * (beta_nz ? 2.0 : 1.0);
   double gemm_bytes = 4.0 * ((double)p.M * p.K + (double)p.K * p.N);
   double reduce = 0.0;

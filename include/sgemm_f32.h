@@ -26,9 +26,11 @@
  *   A, B and C are device pointers owned by the caller (any memory the GPU can address with
  *   a plain load: cudaMalloc, cudaMallocAsync, managed). The library keeps no pointer after
  *   the call returns. C must not overlap A or B.
- *   sgemm_f32 may allocate a split-K workspace with cudaMallocAsync on `stream` and free it
- *   with cudaFreeAsync on the same stream before returning; sgemm_f32_workspace_size()
- *   reports its size and sgemm_f32_ws() takes a caller-provided workspace instead.
+ *   sgemm_f32 may allocate a split-K workspace (at most 64 MiB) with a stream-ordered
+ *   allocation on `stream` and free it on the same stream before returning. It comes from
+ *   a memory pool the library creates per device, which keeps freed memory for reuse until
+ *   the process exits. sgemm_f32_workspace_size() reports the size; sgemm_f32_ws() takes
+ *   a caller-provided workspace instead.
  *
  * Asynchrony
  *   Every compute call enqueues its kernels on `stream` (0 = the legacy default stream) and
