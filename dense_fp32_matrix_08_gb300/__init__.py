@@ -18,13 +18,15 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "LIB_PATH", "SgemmError", "lib", "sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced",
     "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
-    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm", "EXPORTED",
+    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_3xtf32",
+    "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
 EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspace_size",
             "sgemm_f32_plan", "sgemm_f32_num_variants", "sgemm_f32_variant_info",
-            "sgemm_f32_version", "sgemm_f32_noalloc")
+            "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_3xtf32",
+            "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status")
 
 
 class SgemmError(RuntimeError):
@@ -49,6 +51,9 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_ws.argtypes = gemm + [vp, sz, vp]
     L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
     L.sgemm_f32_noalloc.argtypes = gemm + [vp]
+    L.sgemm_f32_3xtf32.argtypes = gemm + [vp]
+    L.sgemm_f32_3xtf32_workspace_size.argtypes = [i, i, i, psz]
+    L.sgemm_f32_3xtf32_status.argtypes = [pi]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
@@ -112,6 +117,25 @@ def sgemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None)
     Returns the C status; -15 means the problem needs more scratch than that array."""
     return lib.sgemm_f32_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
                                  ldc, _stream(stream))
+
+
+def sgemm_f32_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """Tensor-core 3xTF32 variant (same contract and return codes as sgemm_f32)."""
+    return lib.sgemm_f32_3xtf32(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
+                                ldc, _stream(stream))
+
+
+def sgemm_f32_3xtf32_workspace_size(M, N, K) -> tuple[int, int]:
+    b = ctypes.c_size_t(0)
+    rc = lib.sgemm_f32_3xtf32_workspace_size(M, N, K, ctypes.byref(b))
+    return rc, b.value
+
+
+def sgemm_f32_3xtf32_status() -> tuple[int, int]:
+    """(call status, device status word); reading clears the word."""
+    v = ctypes.c_int(0)
+    rc = lib.sgemm_f32_3xtf32_status(ctypes.byref(v))
+    return rc, v.value
 
 
 def sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc) -> tuple[int, int]:

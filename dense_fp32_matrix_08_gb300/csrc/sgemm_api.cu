@@ -11,6 +11,7 @@
 
 #include "../../include/sgemm_f32.h"
 #include "sgemm_aux.cuh"
+#include "sgemm_internal.h"
 #include "sgemm_plan.h"
 #include "sgemm_variants.cuh"
 
@@ -34,7 +35,7 @@ struct DeviceState {
 };
 static DeviceState g_dev[kMaxDevices];
 
-static cudaError_t device_setup(int *num_sms) {
+cudaError_t device_setup(int *num_sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -99,7 +100,7 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   return e.plan;
 }
 
-static cudaMemPool_t workspace_pool() {
+cudaMemPool_t workspace_pool() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   return g_dev[dev].pool;

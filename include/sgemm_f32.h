@@ -167,6 +167,29 @@ int sgemm_f32_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
                       const float *B, int ldb, float beta, float *C, int ldc,
                       cudaStream_t stream);
 
+/* C = alpha * A * B + beta * C on the tensor cores (tcgen05, kind::tf32) with the 3xTF32
+ * split: every FP32 input x is split into x_hi = tf32(x) and x_lo = tf32(x - x_hi) and
+ * A * B is accumulated in FP32 as A_hi B_hi + A_hi B_lo + A_lo B_hi. The dropped terms are
+ * about 2^-21 of each |a b|, so the result meets the same FP32 error bound as sgemm_f32
+ * (1e-4 * sum_k |a_ik b_kj| + |beta c_ij| elementwise) while running on the tensor cores.
+ * Same arguments, layout, special cases and return codes as sgemm_f32. The split operands
+ * live in a workspace of sgemm_f32_3xtf32_workspace_size() bytes that the call takes from
+ * the library's stream-ordered pool and frees on `stream`. Reported separately from the
+ * FFMA path. NaN and Inf inputs are not handled like sgemm_f32 (x - x_hi is NaN for an
+ * infinite x). */
+int sgemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A, int lda,
+                     const float *B, int ldb, float beta, float *C, int ldc,
+                     cudaStream_t stream);
+
+/* Workspace bytes sgemm_f32_3xtf32 uses for an M x N x K problem (host-only query;
+ * negative codes as sgemm_f32 for negative sizes). */
+int sgemm_f32_3xtf32_workspace_size(int M, int N, int K, size_t *bytes);
+
+/* Reads and clears the tensor-core path's device status word (synchronising copy on the
+ * legacy stream): 0 = fine; 1, 2, 3 = a bounded wait of the producer, MMA or epilogue
+ * threads gave up (the kernel then skipped work and the result is not valid). */
+int sgemm_f32_3xtf32_status(int *status);
+
 /* Library version string, e.g. "sgemm_f32 0.1.0 sm_103a". */
 const char *sgemm_f32_version(void);
 
