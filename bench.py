@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle sample")
+    ap.add_argument("--no-variants", action="store_true",
+                    help="skip the separately reported tensor-core 3xTF32 variant")
     ap.add_argument("--variant", type=int, default=-1,
                     help="force a tile configuration (profiling / tuning); -1 = automatic")
     ap.add_argument("--split", type=int, default=0,
@@ -284,6 +286,50 @@ def _config(w):
 
 # ------------------------------------------------------------------------------------
 
+# Dense TF32 tensor peak from the measured bf16 peak and the nominal TF32 : bf16 ratio
+# (1.1 : 2.25 PFLOP/s dense on GB300).
+TF32_OVER_BF16 = 1.1 / 2.25
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+
+
+def tf32_peak_tflops():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return pk["bf16_tflops"] * TF32_OVER_BF16, "of measured (bf16 burst x 1.1/2.25)"
+    except (OSError, ValueError, KeyError):
+        return 1900.0 * TF32_OVER_BF16, "of fallback (1.9 PFLOP/s bf16 x 1.1/2.25)"
+
+
+def tensor_core_variant(sg, args, stream, w, dA, dB, dC, C0):
+    """The 3xTF32 tensor-core variant on the same workload, reported separately: FP32-
+    equivalent TFLOP/s (2MNK/t, split passes included) and its tensor roofline (3 TF32
+    products per multiply-add against the TF32 peak)."""
+    M, N, K = w.M, w.N, w.K
+    s_handle = stream.cuda_stream
+    dC.copy_(C0)
+
+    def step():
+        rc = sg.lib.sgemm_f32_3xtf32(M, N, K, w.alpha, dA.data_ptr(), K, dB.data_ptr(), N,
+                                     w.beta, dC.data_ptr(), N, s_handle)
+        if rc != 0:
+            raise RuntimeError(f"sgemm_f32_3xtf32 returned {rc}")
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        t = time_steps(step, args.steps, stream)
+    rc, status = sg.sgemm_f32_3xtf32_status()
+    value = w.flops * args.steps / t / 1e12
+    peak, basis = tf32_peak_tflops()
+    return {"value": value, "unit": UNIT, "ms_per_step": 1e3 * t / args.steps,
+            "launches_per_step": 3, "device_status": status,
+            "roofline": {"bound": "tensor", "achieved": 3 * value, "peak": peak,
+                         "unit": "TFLOP/s", "frac": 3 * value / peak, "peak_basis": basis,
+                         "note": "achieved counts the 3 TF32 products per multiply-add; "
+                                 "the time includes the hi/lo split passes"}}
+
+
 def time_steps(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -427,6 +473,10 @@ def our_arm(args, dist: Dist):
                               "launches_per_step": p2["launches"],
                               "l2": "inputs 201 MB > L2 (no flush)"}
 
+    variants = {}
+    if not args.no_variants:
+        variants["3xtf32_tensor_core"] = tensor_core_variant(sg, args, stream, w, dA, dB, dC, C0)
+
     if dist.rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
@@ -441,6 +491,8 @@ def our_arm(args, dist: Dist):
         }
         if secondary:
             line["secondary"] = secondary
+        if variants:
+            line["variants"] = variants
         print(json.dumps(line), flush=True)
 
 
