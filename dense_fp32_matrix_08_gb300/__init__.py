@@ -18,14 +18,16 @@ from ._build import LIB as LIB_PATH
 __all__ = [
     "LIB_PATH", "SgemmError", "lib", "sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced",
     "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
-    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_3xtf32",
+    "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex",
+    "sgemm_f32_colmajor", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
 EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspace_size",
             "sgemm_f32_plan", "sgemm_f32_num_variants", "sgemm_f32_variant_info",
-            "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_3xtf32",
+            "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex", "sgemm_f32_colmajor",
+            "sgemm_f32_3xtf32",
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status")
 
 
@@ -51,6 +53,8 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_ws.argtypes = gemm + [vp, sz, vp]
     L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
     L.sgemm_f32_noalloc.argtypes = gemm + [vp]
+    L.sgemm_f32_ex.argtypes = [i, i] + gemm + [vp]
+    L.sgemm_f32_colmajor.argtypes = [i, i] + gemm + [vp]
     L.sgemm_f32_3xtf32.argtypes = gemm + [vp]
     L.sgemm_f32_3xtf32_workspace_size.argtypes = [i, i, i, psz]
     L.sgemm_f32_3xtf32_status.argtypes = [pi]
@@ -117,6 +121,20 @@ def sgemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None)
     Returns the C status; -15 means the problem needs more scratch than that array."""
     return lib.sgemm_f32_noalloc(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
                                  ldc, _stream(stream))
+
+
+def sgemm_f32_ex(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc,
+                 stream=None) -> int:
+    """Row-major C = alpha op(A) op(B) + beta C with transpose flags (0 = N, 1 = T)."""
+    return lib.sgemm_f32_ex(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, _ptr(B),
+                            ldb, beta, _ptr(C), ldc, _stream(stream))
+
+
+def sgemm_f32_colmajor(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, ldc,
+                       stream=None) -> int:
+    """Column-major BLAS-style sgemm (transa/transb: 0 = N, 1 = T)."""
+    return lib.sgemm_f32_colmajor(int(transa), int(transb), m, n, k, alpha, _ptr(A), lda,
+                                  _ptr(B), ldb, beta, _ptr(C), ldc, _stream(stream))
 
 
 def sgemm_f32_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

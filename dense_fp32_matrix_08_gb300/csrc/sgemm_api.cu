@@ -45,9 +45,12 @@ cudaError_t device_setup(int *num_sms) {
     int sms = 0;
     cudaError_t err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     for (int v = 0; v < kNumVariants && err == cudaSuccess; ++v)
-      for (int a = 0; a < 2 && err == cudaSuccess; ++a)
-        err = cudaFuncSetAttribute(kKernels[v].k[a], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   kKernels[v].smem);
+      for (int a = 0; a < 3 && err == cudaSuccess; ++a)
+        for (int b = 0; b < 3 && err == cudaSuccess; ++b)
+          if (kKernels[v].k[a][b])
+            err = cudaFuncSetAttribute(kKernels[v].k[a][b],
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kKernels[v].smem);
     // A pool of the library's own for split-K workspaces. It keeps freed memory (release
     // threshold: never), so a stream-ordered allocation of a recently freed size is a
     // cheap reuse instead of a fresh mapping; the default pool returns its memory at every
@@ -78,7 +81,7 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
                         int force_split) {
   struct Entry {
     int M, N, K, num_sms, force_v, force_split;
-    unsigned flags;
+    unsigned flags;  // alpha == 0, beta != 0, beta == 1, op(A) transposed, op(B) transposed
     bool valid;
     Plan plan;
   };
@@ -86,7 +89,8 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   thread_local Entry cache[kEntries] = {};
   thread_local int next = 0;
   const unsigned flags = (alpha == 0.0f ? 1u : 0u) | (beta != 0.0f ? 2u : 0u) |
-                         (beta == 1.0f ? 4u : 0u);
+                         (beta == 1.0f ? 4u : 0u) | (pr.transa ? 8u : 0u) |
+                         (pr.transb ? 16u : 0u);
   for (int i = 0; i < kEntries; ++i) {
     const Entry &e = cache[i];
     if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
@@ -149,9 +153,14 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   p.tiles_n = pl.tiles_n;
   p.group_m = pl.group_m;
   p.vec_c = vec_c ? 1 : 0;
-  const bool vec_b = (pr.ldb % 4 == 0) && aligned16(B);
+  const int apath = !pr.transa ? APATH_N
+                    : ((pr.lda % 4 == 0) && aligned16(A)) ? APATH_T16 : APATH_T4;
+  const int bpath = pr.transb ? BPATH_T
+                    : ((pr.ldb % 4 == 0) && aligned16(B)) ? BPATH_N16 : BPATH_N4;
+  const KernelFn fn = kKernels[pl.variant].k[apath][bpath];
+  if (fn == nullptr) return kErrBadVariant;  // forced variant without transposed paths
   if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
-  kKernels[pl.variant].k[vec_b]<<<pl.ctas, vs.threads, vs.smem_bytes, stream>>>(p);
+  fn<<<pl.ctas, vs.threads, vs.smem_bytes, stream>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   const long long tail_tiles = (long long)pl.tiles_m * pl.tiles_n - pl.main_tiles;
@@ -170,9 +179,10 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
 static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda,
                        const float *B, int ldb, float beta, float *C, int ldc, int force_v,
                        int force_split, int ws_mode, void *ws, size_t ws_bytes,
-                       cudaStream_t stream) {
-  Problem pr{M, N, K, lda, ldb, ldc};
-  int rc = validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
+                       cudaStream_t stream, int transa = 0, int transb = 0) {
+  Problem pr{M, N, K, lda, ldb, ldc, transa, transb};
+  int rc = (transa || transb) ? validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr)
+                              : validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
   if (rc != 0) return rc;
   if (M == 0 || N == 0) return 0;
   if (force_v >= kNumVariants || force_v < -1) return kErrBadVariant;
@@ -209,6 +219,31 @@ int sgemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const f
               int ldb, float beta, float *C, int ldc, cudaStream_t stream) {
   return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, -1, 0, 0, nullptr, 0,
                      stream);
+}
+
+int sgemm_f32_ex(int transa, int transb, int M, int N, int K, float alpha, const float *A,
+                 int lda, const float *B, int ldb, float beta, float *C, int ldc,
+                 cudaStream_t stream) {
+  Problem pr{M, N, K, lda, ldb, ldc, transa, transb};
+  const int rc = validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
+  if (rc != 0) return rc;
+  return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, -1, 0, 0, nullptr, 0,
+                     stream, transa, transb);
+}
+
+// Column-major C (m x n) = alpha op(A) op(B) + beta C is, read row-major, the n x m matrix
+// C^T = alpha op(B)^T op(A)^T + beta C^T: the same call with the operands swapped and
+// each operand's transpose flag applied to its row-major view ("Lecture 4 - GPU
+// Acceleration", section 5.4, the swap trick for calling a column-major library on
+// row-major tensors, used here the other way round).
+int sgemm_f32_colmajor(int transa, int transb, int m, int n, int k, float alpha,
+                       const float *A, int lda, const float *B, int ldb, float beta, float *C,
+                       int ldc, cudaStream_t stream) {
+  const int rc = validate_colmajor(transa, transb, m, n, k, lda, ldb, ldc, alpha,
+                                   A != nullptr, B != nullptr, C != nullptr);
+  if (rc != 0) return rc;
+  return sgemm_entry(n, m, k, alpha, B, ldb, A, lda, beta, C, ldc, -1, 0, 0, nullptr, 0, stream,
+                     transb, transa);
 }
 
 int sgemm_f32_ws(int M, int N, int K, float alpha, const float *A, int lda, const float *B,

@@ -122,8 +122,17 @@ struct TileConfig {
   static constexpr int B_CHUNKS = BK * BN / 4;
   static constexpr int B_ITERS_VEC = B_CHUNKS / NT;
   static constexpr int B_ITERS_SCALAR = BK * BN / NT;
-  // XOR swizzle of As chunk index: low bits flipped by k.
+  // XOR swizzle of the As and Bs chunk indices: low bits flipped by k.
   static constexpr int SWZ = (BM * AW / 4 >= 8) ? 7 : (BM * AW / 4 - 1);
+  static constexpr int SWZB = (BN / 4 >= 8) ? 7 : (BN / 4 - 1);
+  // Copies for transposed operands (op(A) = A_st^T with A_st K x M, op(B) = B_st^T with
+  // B_st N x K, both row-major): A_st rows are already As rows (16- or 4-byte copies);
+  // B_st is transposed into Bs by 4-byte copies, one 8 (k) x 4 (n) block per warp
+  // instruction, like the A copy of the non-transposed path.
+  static constexpr int AT_ITERS_VEC = BK * BM / 4 / NT;
+  static constexpr int AT_ITERS_SCALAR = BK * BM / NT;
+  static constexpr int BT_BLOCKS = (BK / 8) * (BN / 4);
+  static constexpr int BT_ITERS = BT_BLOCKS / NWARPS;
 
   static_assert(BM % WM == 0 && BN % WN == 0, "warp tiles must divide the CTA tile");
   static_assert(LM * LN == 32, "a warp is 32 lanes");
@@ -158,6 +167,24 @@ __device__ __forceinline__ int a_phys(int k, int m, int dup) {
   }
 }
 
+// Physical float index of column n inside one Bs row (fixed k): the 16-byte chunk index is
+// XOR-swizzled with k, so both the row-wise 16-byte copies and the transposing 4-byte
+// copies (8 k x 4 n per warp instruction) hit 32 distinct banks.
+template <class Cfg>
+__device__ __forceinline__ int b_phys(int k, int n) {
+  return (((n >> 2) ^ (k & Cfg::SWZB)) << 2) | (n & 3);
+}
+
+// Operand copy paths of the GEMM kernel.
+//   A: APATH_N   A is M x K row-major, transposed into As by 4-byte copies;
+//      APATH_T16 op(A) = A_st^T, A_st K x M row-major, 16-byte copies (lda % 4 == 0);
+//      APATH_T4  the same layout with 4-byte copies.
+//   B: BPATH_N4  B is K x N row-major, 4-byte copies;
+//      BPATH_N16 the same with 16-byte copies (ldb % 4 == 0);
+//      BPATH_T   op(B) = B_st^T, B_st N x K row-major, transposed into Bs by 4-byte copies.
+enum { APATH_N = 0, APATH_T16 = 1, APATH_T4 = 2 };
+enum { BPATH_N4 = 0, BPATH_N16 = 1, BPATH_T = 2 };
+
 // d = a * b + c on register pairs {lo, hi} (two independent FP32 FMAs, round to nearest).
 __device__ __forceinline__ void ffma2(unsigned long long &d, unsigned long long a,
                                       unsigned long long b) {
@@ -189,9 +216,15 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
   tn = in_group / rows;
 }
 
-template <class Cfg, bool VEC_B>
+template <class Cfg, int APATH, int BPATH>
 __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const GemmParams p) {
+  static_assert(APATH == APATH_N || Cfg::MODE != 2, "duplicated-A layout needs A row-major");
+  static_assert(APATH != APATH_T16 || (Cfg::BK * Cfg::BM / 4) % Cfg::NT == 0, "A^T 16B tiling");
+  static_assert(APATH != APATH_T4 || (Cfg::BK * Cfg::BM) % Cfg::NT == 0, "A^T 4B tiling");
+  static_assert(BPATH != BPATH_T || (Cfg::BT_BLOCKS % Cfg::NWARPS == 0 &&
+                                     Cfg::NWARPS % (Cfg::BK / 8) == 0),
+                "B^T copy blocks must split evenly over warps");
   constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
   constexpr int TM = Cfg::TM, TN = Cfg::TN, LM = Cfg::LM, LN = Cfg::LN;
   constexpr int FM = Cfg::FM, FN = Cfg::FN, NT = Cfg::NT, NWARPS = Cfg::NWARPS;
@@ -248,22 +281,48 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
 
   auto load_tile = [&](int kt, int slot) {
     const int k0 = k_begin + kt * BK;
-    // A, transposed on the fly into As[slot][k][a_phys(m)]
-    float *as = As + slot * Cfg::A_STAGE + a_k * AROW;
-    const int kg = k0 + a_k;
-    const bool k_ok = kg < k_end;
+    float *as_stage = As + slot * Cfg::A_STAGE;
+    if constexpr (APATH == APATH_N) {
+      // A, transposed on the fly into As[slot][k][a_phys(m)]
+      float *as = as_stage + a_k * AROW;
+      const int kg = k0 + a_k;
+      const bool k_ok = kg < k_end;
 #pragma unroll
-    for (int it = 0; it < Cfg::A_ITERS; ++it) {
-      const int m = a_m_base + it * A_M_STEP;
-      const int mg = m0 + m;
-      const bool ok = k_ok && (mg < p.M);
-      const float *src = ok ? p.A + (long long)mg * p.lda + kg : p.A;
-      cp_async_4(smem_addr(as + a_phys<Cfg>(a_k, m, 0)), src, ok ? 4 : 0);
-      if constexpr (MODE == 2)
-        cp_async_4(smem_addr(as + a_phys<Cfg>(a_k, m, 1)), src, ok ? 4 : 0);
+      for (int it = 0; it < Cfg::A_ITERS; ++it) {
+        const int m = a_m_base + it * A_M_STEP;
+        const int mg = m0 + m;
+        const bool ok = k_ok && (mg < p.M);
+        const float *src = ok ? p.A + (long long)mg * p.lda + kg : p.A;
+        cp_async_4(smem_addr(as + a_phys<Cfg>(a_k, m, 0)), src, ok ? 4 : 0);
+        if constexpr (MODE == 2)
+          cp_async_4(smem_addr(as + a_phys<Cfg>(a_k, m, 1)), src, ok ? 4 : 0);
+      }
+    } else if constexpr (APATH == APATH_T16) {
+      // rows of A_st (fixed k) are rows of As: 16-byte chunks of 4 consecutive m
+#pragma unroll
+      for (int it = 0; it < Cfg::AT_ITERS_VEC; ++it) {
+        const int q = it * NT + tid;
+        const int kk = q / (BM / 4);
+        const int mc = (q % (BM / 4)) * 4;
+        const int kg = k0 + kk, mg = m0 + mc;
+        const int bytes = (kg < k_end) ? max(0, min(4, p.M - mg)) * 4 : 0;
+        const float *src = bytes ? p.A + (long long)kg * p.lda + mg : p.A;
+        cp_async_16(smem_addr(as_stage + kk * AROW + a_phys<Cfg>(kk, mc, 0)), src, bytes);
+      }
+    } else {
+#pragma unroll
+      for (int it = 0; it < Cfg::AT_ITERS_SCALAR; ++it) {
+        const int q = it * NT + tid;
+        const int kk = q / BM;
+        const int mm = q % BM;
+        const int kg = k0 + kk, mg = m0 + mm;
+        const bool ok = (kg < k_end) && (mg < p.M);
+        const float *src = ok ? p.A + (long long)kg * p.lda + mg : p.A;
+        cp_async_4(smem_addr(as_stage + kk * AROW + a_phys<Cfg>(kk, mm, 0)), src, ok ? 4 : 0);
+      }
     }
     float *bs = Bs + slot * Cfg::B_STAGE;
-    if constexpr (VEC_B) {
+    if constexpr (BPATH == BPATH_N16) {
       const int ng = n0 + bv_n;
       const int n_bytes = max(0, min(4, p.N - ng)) * 4;
 #pragma unroll
@@ -272,9 +331,9 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
         const int kgb = k0 + kk;
         const int bytes = (kgb < k_end) ? n_bytes : 0;
         const float *src = bytes ? p.B + (long long)kgb * p.ldb + ng : p.B;
-        cp_async_16(smem_addr(bs + kk * BN + bv_n), src, bytes);
+        cp_async_16(smem_addr(bs + kk * BN + b_phys<Cfg>(kk, bv_n)), src, bytes);
       }
-    } else {
+    } else if constexpr (BPATH == BPATH_N4) {
 #pragma unroll
       for (int it = 0; it < Cfg::B_ITERS_SCALAR; ++it) {
         const int q = it * NT + tid;
@@ -284,7 +343,21 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
         const int ng = n0 + nn;
         const bool ok = (kgb < k_end) && (ng < p.N);
         const float *src = ok ? p.B + (long long)kgb * p.ldb + ng : p.B;
-        cp_async_4(smem_addr(bs + kk * BN + nn), src, ok ? 4 : 0);
+        cp_async_4(smem_addr(bs + kk * BN + b_phys<Cfg>(kk, nn)), src, ok ? 4 : 0);
+      }
+    } else {
+      // B_st (N x K) transposed into Bs[k][b_phys(n)]: 8 consecutive k of 4 rows n per
+      // warp instruction (coalesced 32-byte row segments, conflict-free smem writes)
+      const int kk = (warp % KB) * 8 + (lane & 7);
+      const int kg = k0 + kk;
+      const bool k_ok = kg < k_end;
+#pragma unroll
+      for (int it = 0; it < Cfg::BT_ITERS; ++it) {
+        const int nn = (it * (NWARPS / KB) + warp / KB) * 4 + (lane >> 3);
+        const int ng = n0 + nn;
+        const bool ok = k_ok && (ng < p.N);
+        const float *src = ok ? p.B + (long long)ng * p.ldb + kg : p.B;
+        cp_async_4(smem_addr(bs + kk * BN + b_phys<Cfg>(kk, nn)), src, ok ? 4 : 0);
       }
     }
   };
@@ -328,7 +401,8 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     }
 #pragma unroll
     for (int c = 0; c < FN; ++c)
-      fb[buf][c] = *reinterpret_cast<const float4 *>(bs + k * BN + b_col0 + c * LN * 4);
+      fb[buf][c] = *reinterpret_cast<const float4 *>(bs + k * BN +
+                                                      b_phys<Cfg>(k, b_col0 + c * LN * 4));
   };
 
   // ---- main loop ----------------------------------------------------------------------

@@ -2,9 +2,9 @@
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
-template <> VariantKernels variant_kernels<0>() { return make_kernels<VariantCfg<0>::type>(); }
-template <> VariantKernels variant_kernels<1>() { return make_kernels<VariantCfg<1>::type>(); }
-template <> VariantKernels variant_kernels<2>() { return make_kernels<VariantCfg<2>::type>(); }
-template <> VariantKernels variant_kernels<3>() { return make_kernels<VariantCfg<3>::type>(); }
-template <> VariantKernels variant_kernels<4>() { return make_kernels<VariantCfg<4>::type>(); }
+SGEMM_DEFINE_VARIANT(0)
+SGEMM_DEFINE_VARIANT(1)
+SGEMM_DEFINE_VARIANT(2)
+SGEMM_DEFINE_VARIANT(3)
+SGEMM_DEFINE_VARIANT(4)
 }  // namespace sgemm

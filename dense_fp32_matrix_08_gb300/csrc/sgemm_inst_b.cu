@@ -2,7 +2,7 @@
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
-template <> VariantKernels variant_kernels<5>() { return make_kernels<VariantCfg<5>::type>(); }
-template <> VariantKernels variant_kernels<6>() { return make_kernels<VariantCfg<6>::type>(); }
-template <> VariantKernels variant_kernels<7>() { return make_kernels<VariantCfg<7>::type>(); }
+SGEMM_DEFINE_VARIANT(5)
+SGEMM_DEFINE_VARIANT(6)
+SGEMM_DEFINE_VARIANT(7)
 }  // namespace sgemm

@@ -2,7 +2,7 @@
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
-template <> VariantKernels variant_kernels<8>() { return make_kernels<VariantCfg<8>::type>(); }
-template <> VariantKernels variant_kernels<9>() { return make_kernels<VariantCfg<9>::type>(); }
-template <> VariantKernels variant_kernels<10>() { return make_kernels<VariantCfg<10>::type>(); }
+SGEMM_DEFINE_VARIANT(8)
+SGEMM_DEFINE_VARIANT(9)
+SGEMM_DEFINE_VARIANT(10)
 }  // namespace sgemm

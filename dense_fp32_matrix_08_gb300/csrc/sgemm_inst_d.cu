@@ -2,7 +2,7 @@
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
-template <> VariantKernels variant_kernels<11>() { return make_kernels<VariantCfg<11>::type>(); }
-template <> VariantKernels variant_kernels<12>() { return make_kernels<VariantCfg<12>::type>(); }
-template <> VariantKernels variant_kernels<13>() { return make_kernels<VariantCfg<13>::type>(); }
+SGEMM_DEFINE_VARIANT(11)
+SGEMM_DEFINE_VARIANT(12)
+SGEMM_DEFINE_VARIANT(13)
 }  // namespace sgemm

@@ -2,8 +2,8 @@
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
-template <> VariantKernels variant_kernels<14>() { return make_kernels<VariantCfg<14>::type>(); }
-template <> VariantKernels variant_kernels<15>() { return make_kernels<VariantCfg<15>::type>(); }
-template <> VariantKernels variant_kernels<16>() { return make_kernels<VariantCfg<16>::type>(); }
-template <> VariantKernels variant_kernels<17>() { return make_kernels<VariantCfg<17>::type>(); }
+SGEMM_DEFINE_VARIANT(14)
+SGEMM_DEFINE_VARIANT(15)
+SGEMM_DEFINE_VARIANT(16)
+SGEMM_DEFINE_VARIANT(17)
 }  // namespace sgemm

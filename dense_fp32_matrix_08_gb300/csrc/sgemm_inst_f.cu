@@ -1,7 +1,9 @@
-// Kernel instantiations of tile configurations 18 19 (see sgemm_variants.cuh).
+// Kernel instantiations of tile configurations 18 19 20 21 (see sgemm_variants.cuh).
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
-template <> VariantKernels variant_kernels<18>() { return make_kernels<VariantCfg<18>::type>(); }
-template <> VariantKernels variant_kernels<19>() { return make_kernels<VariantCfg<19>::type>(); }
+SGEMM_DEFINE_VARIANT(18)
+SGEMM_DEFINE_VARIANT(19)
+SGEMM_DEFINE_VARIANT(20)
+SGEMM_DEFINE_VARIANT(21)
 }  // namespace sgemm

@@ -15,6 +15,7 @@ constexpr int kErrBadVariant = -14;
 
 struct Problem {
   int M, N, K, lda, ldb, ldc;
+  int transa = 0, transb = 0;  // 1: op(X) = X_st^T (see sgemm_f32_ex)
 };
 
 // Shape of one compiled tile configuration (mirrors TileConfig in sgemm_ffma.cuh).
@@ -22,6 +23,7 @@ struct VariantShape {
   int BM, BN, BK, threads, TM, TN, stages, min_blocks, mode, smem_bytes;
   double eff;  // modelled fraction of the FP32 pipe this configuration sustains
   bool automatic;  // considered by the automatic plan (others only when forced)
+  bool trans_ok;   // compiled with the transposed-operand copy paths
 };
 
 // mode: 0 scalar FFMA, 1 FFMA2 with register broadcast, 2 FFMA2 with duplicated A in smem
@@ -30,26 +32,28 @@ constexpr int smem_of(int BM, int BN, int BK, int stages, int mode) {
 }
 
 constexpr VariantShape kVariants[] = {
-    {128, 256, 16, 256, 16, 8, 3, 1, 0, smem_of(128, 256, 16, 3, 0), 0.78, true},
-    {128, 128, 16, 256, 8, 8, 4, 2, 0, smem_of(128, 128, 16, 4, 0), 0.72, true},
-    {64, 64, 16, 128, 8, 4, 4, 4, 0, smem_of(64, 64, 16, 4, 0), 0.60, true},
-    {16, 256, 32, 128, 8, 4, 3, 2, 0, smem_of(16, 256, 32, 3, 0), 0.50, true},
-    {256, 16, 32, 128, 8, 4, 3, 2, 0, smem_of(256, 16, 32, 3, 0), 0.50, true},
-    {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.86, true},
-    {128, 256, 16, 256, 8, 16, 3, 1, 2, smem_of(128, 256, 16, 3, 2), 0.80, false},
-    {128, 256, 32, 256, 8, 16, 3, 1, 2, smem_of(128, 256, 32, 3, 2), 0.80, false},
-    {128, 128, 16, 256, 8, 8, 4, 2, 1, smem_of(128, 128, 16, 4, 1), 0.83, true},
-    {128, 256, 16, 512, 8, 8, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false},
-    {256, 128, 16, 512, 8, 8, 3, 1, 1, smem_of(256, 128, 16, 3, 1), 0.80, false},
-    {128, 256, 32, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 32, 3, 1), 0.80, false},
-    {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false},
-    {128, 256, 16, 256, 8, 16, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.88, true},
-    {128, 64, 16, 128, 8, 8, 3, 2, 1, smem_of(128, 64, 16, 3, 1), 0.80, false},
-    {128, 64, 16, 128, 8, 8, 4, 2, 1, smem_of(128, 64, 16, 4, 1), 0.80, false},
-    {128, 128, 16, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.90, true},
-    {128, 64, 16, 128, 8, 8, 3, 3, 1, smem_of(128, 64, 16, 3, 1), 0.80, false},
-    {128, 256, 16, 256, 4, 32, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.80, false},
-    {128, 128, 16, 128, 4, 32, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.80, false},
+    {128, 256, 16, 256, 16, 8, 3, 1, 0, smem_of(128, 256, 16, 3, 0), 0.78, true, false},
+    {128, 128, 16, 256, 8, 8, 4, 2, 0, smem_of(128, 128, 16, 4, 0), 0.72, true, false},
+    {64, 64, 16, 128, 8, 4, 4, 4, 0, smem_of(64, 64, 16, 4, 0), 0.60, true, true},
+    {16, 256, 32, 128, 8, 4, 3, 2, 0, smem_of(16, 256, 32, 3, 0), 0.50, true, true},
+    {256, 16, 32, 128, 8, 4, 3, 2, 0, smem_of(256, 16, 32, 3, 0), 0.50, true, true},
+    {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.86, true, false},
+    {128, 256, 16, 256, 8, 16, 3, 1, 2, smem_of(128, 256, 16, 3, 2), 0.80, false, false},
+    {128, 256, 32, 256, 8, 16, 3, 1, 2, smem_of(128, 256, 32, 3, 2), 0.80, false, false},
+    {128, 128, 16, 256, 8, 8, 4, 2, 1, smem_of(128, 128, 16, 4, 1), 0.83, true, false},
+    {128, 256, 16, 512, 8, 8, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false, false},
+    {256, 128, 16, 512, 8, 8, 3, 1, 1, smem_of(256, 128, 16, 3, 1), 0.80, false, false},
+    {128, 256, 32, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 32, 3, 1), 0.80, false, false},
+    {128, 256, 16, 256, 8, 16, 3, 1, 1, smem_of(128, 256, 16, 3, 1), 0.80, false, false},
+    {128, 256, 16, 256, 8, 16, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.88, true, false},
+    {128, 64, 16, 128, 8, 8, 3, 2, 1, smem_of(128, 64, 16, 3, 1), 0.80, false, false},
+    {128, 64, 16, 128, 8, 8, 4, 2, 1, smem_of(128, 64, 16, 4, 1), 0.80, false, false},
+    {128, 128, 16, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.90, true, true},
+    {128, 64, 16, 128, 8, 8, 3, 3, 1, smem_of(128, 64, 16, 3, 1), 0.80, false, false},
+    {128, 256, 16, 256, 4, 32, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.80, false, false},
+    {128, 128, 16, 128, 4, 32, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.80, false, false},
+    {16, 512, 16, 128, 8, 8, 3, 2, 1, smem_of(16, 512, 16, 3, 1), 0.60, false, false},
+    {128, 16, 32, 128, 4, 4, 4, 3, 0, smem_of(128, 16, 32, 4, 0), 0.50, false, false},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -71,6 +75,8 @@ inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 // BLAS-style check: the first illegal argument, numbered from 1 in the sgemm_f32 order
 // (M, N, K, alpha, A, lda, B, ldb, beta, C, ldc). A and B only have to be present when
 // they are read (alpha != 0, K > 0, non-empty C); C whenever the view is non-empty.
+// With transposed operands the stored A is K x M (lda >= M) and the stored B is N x K
+// (ldb >= K), row-major.
 inline int validate(const Problem &p, float alpha, bool hasA, bool hasB, bool hasC) {
   if (p.M < 0) return -1;
   if (p.N < 0) return -2;
@@ -78,11 +84,40 @@ inline int validate(const Problem &p, float alpha, bool hasA, bool hasB, bool ha
   const bool nonempty = p.M > 0 && p.N > 0;
   const bool reads_ab = nonempty && p.K > 0 && alpha != 0.0f;
   if (reads_ab && !hasA) return -5;
-  if (p.lda < std::max(1, p.K)) return -6;
+  if (p.lda < std::max(1, p.transa ? p.M : p.K)) return -6;
   if (reads_ab && !hasB) return -7;
-  if (p.ldb < std::max(1, p.N)) return -8;
+  if (p.ldb < std::max(1, p.transb ? p.K : p.N)) return -8;
   if (nonempty && !hasC) return -10;
   if (p.ldc < std::max(1, p.N)) return -11;
+  return 0;
+}
+
+// sgemm_f32_ex order: (transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc).
+inline int validate_ex(const Problem &p, float alpha, bool hasA, bool hasB, bool hasC) {
+  if (p.transa != 0 && p.transa != 1) return -1;
+  if (p.transb != 0 && p.transb != 1) return -2;
+  const int rc = validate(p, alpha, hasA, hasB, hasC);
+  return rc < 0 ? rc - 2 : rc;
+}
+
+// Column-major (BLAS / cuBLAS) order and rules: (transa, transb, m, n, k, alpha, A, lda,
+// B, ldb, beta, C, ldc); A is m x k (k x m when transposed), B is k x n (n x k), C m x n,
+// each with ld >= its row count.
+inline int validate_colmajor(int transa, int transb, int m, int n, int k, int lda, int ldb,
+                             int ldc, float alpha, bool hasA, bool hasB, bool hasC) {
+  if (transa != 0 && transa != 1) return -1;
+  if (transb != 0 && transb != 1) return -2;
+  if (m < 0) return -3;
+  if (n < 0) return -4;
+  if (k < 0) return -5;
+  const bool nonempty = m > 0 && n > 0;
+  const bool reads_ab = nonempty && k > 0 && alpha != 0.0f;
+  if (reads_ab && !hasA) return -7;
+  if (lda < std::max(1, transa ? k : m)) return -8;
+  if (reads_ab && !hasB) return -9;
+  if (ldb < std::max(1, transb ? n : k)) return -10;
+  if (nonempty && !hasC) return -12;
+  if (ldc < std::max(1, m)) return -13;
   return 0;
 }
 
@@ -188,8 +223,10 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   };
   const int v_lo = force_v >= 0 ? force_v : 0;
   const int v_hi = force_v >= 0 ? force_v : kNumVariants - 1;
+  const bool trans = p.transa || p.transb;
   for (int v = v_lo; v <= v_hi; ++v) {
     if (force_v < 0 && !kVariants[v].automatic) continue;
+    if (trans && !kVariants[v].trans_ok) continue;
     const VariantShape &s = kVariants[v];
     const long long tiles = ceil_div(p.M, s.BM) * ceil_div(p.N, s.BN);
     const long long kt = ceil_div(p.K, s.BK);

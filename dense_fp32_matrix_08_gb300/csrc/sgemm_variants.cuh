@@ -12,7 +12,7 @@ namespace sgemm {
 using KernelFn = void (*)(const GemmParams);
 
 struct VariantKernels {
-  KernelFn k[2];  // [vec_b]
+  KernelFn k[3][3];  // [APATH][BPATH]; null where not instantiated
   int threads;
   int smem;
 };
@@ -41,10 +41,12 @@ template <> struct VariantCfg<16> { using type = TileConfig<128, 128, 16, 64, 64
 template <> struct VariantCfg<17> { using type = TileConfig<128, 64, 16, 64, 32, 8, 8, 3, 3, 1>; };
 template <> struct VariantCfg<18> { using type = TileConfig<128, 256, 16, 32, 128, 4, 32, 4, 1, 1>; };
 template <> struct VariantCfg<19> { using type = TileConfig<128, 128, 16, 32, 128, 4, 32, 3, 2, 1>; };
+template <> struct VariantCfg<20> { using type = TileConfig<16, 512, 16, 16, 128, 8, 8, 3, 2, 1>; };
+template <> struct VariantCfg<21> { using type = TileConfig<128, 16, 32, 32, 16, 4, 4, 4, 3, 0>; };
 
 #define SGEMM_FOR_EACH_VARIANT(X) \
   X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) \
-  X(16) X(17) X(18) X(19)
+  X(16) X(17) X(18) X(19) X(20) X(21)
 
 template <class Cfg>
 constexpr bool matches(const VariantShape &s) {
@@ -61,11 +63,32 @@ constexpr bool matches(const VariantShape &s) {
 SGEMM_FOR_EACH_VARIANT(SGEMM_CHECK_VARIANT)
 #undef SGEMM_CHECK_VARIANT
 
-template <class Cfg>
+// Every configuration gets the row-major paths (A as given; B with 4- or 16-byte copies);
+// configurations marked trans_ok in kVariants also get the transposed-operand paths.
+template <class Cfg, bool TRANS>
 VariantKernels make_kernels() {
-  return VariantKernels{{sgemm_ffma_kernel<Cfg, false>, sgemm_ffma_kernel<Cfg, true>},
-                        Cfg::NT, Cfg::SMEM_BYTES};
+  VariantKernels vk = {};
+  vk.threads = Cfg::NT;
+  vk.smem = Cfg::SMEM_BYTES;
+  vk.k[APATH_N][BPATH_N4] = sgemm_ffma_kernel<Cfg, APATH_N, BPATH_N4>;
+  vk.k[APATH_N][BPATH_N16] = sgemm_ffma_kernel<Cfg, APATH_N, BPATH_N16>;
+  if constexpr (TRANS) {
+    vk.k[APATH_N][BPATH_T] = sgemm_ffma_kernel<Cfg, APATH_N, BPATH_T>;
+    vk.k[APATH_T16][BPATH_N4] = sgemm_ffma_kernel<Cfg, APATH_T16, BPATH_N4>;
+    vk.k[APATH_T16][BPATH_N16] = sgemm_ffma_kernel<Cfg, APATH_T16, BPATH_N16>;
+    vk.k[APATH_T16][BPATH_T] = sgemm_ffma_kernel<Cfg, APATH_T16, BPATH_T>;
+    vk.k[APATH_T4][BPATH_N4] = sgemm_ffma_kernel<Cfg, APATH_T4, BPATH_N4>;
+    vk.k[APATH_T4][BPATH_N16] = sgemm_ffma_kernel<Cfg, APATH_T4, BPATH_N16>;
+    vk.k[APATH_T4][BPATH_T] = sgemm_ffma_kernel<Cfg, APATH_T4, BPATH_T>;
+  }
+  return vk;
 }
+
+#define SGEMM_DEFINE_VARIANT(v)                                                        \
+  template <>                                                                          \
+  VariantKernels variant_kernels<v>() {                                                \
+    return make_kernels<VariantCfg<v>::type, kVariants[v].trans_ok>();                 \
+  }
 
 // Defined in the sgemm_inst_*.cu files.
 template <int V>

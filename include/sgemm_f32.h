@@ -81,6 +81,29 @@ typedef struct CUstream_st *cudaStream_t;
 int sgemm_f32(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
               int ldb, float beta, float *C, int ldc, cudaStream_t stream);
 
+/* C = alpha * op(A) * op(B) + beta * C, row-major, with BLAS transpose flags ("Lecture 4 -
+ * GPU Acceleration", section 5.2: op(X) is X or X^T). transa / transb: 0 = as stored,
+ * 1 = transposed. C is M x N (ldc >= max(1, N)); op(A) is M x K and op(B) is K x N:
+ *   transa = 0: A stored M x K, lda >= max(1, K);  transa = 1: A stored K x M, lda >= max(1, M)
+ *   transb = 0: B stored K x N, ldb >= max(1, N);  transb = 1: B stored N x K, ldb >= max(1, K)
+ * (all row-major). Same memory, asynchrony and special cases as sgemm_f32. Returns 0, or
+ * -i for the first illegal argument in this signature's order (transa = 1, transb = 2,
+ * M = 3, ..., ldc = 13), or a cudaError_t. */
+int sgemm_f32_ex(int transa, int transb, int M, int N, int K, float alpha, const float *A,
+                 int lda, const float *B, int ldb, float beta, float *C, int ldc,
+                 cudaStream_t stream);
+
+/* Column-major interface with the BLAS sgemm argument list (as cuBLAS takes it, with the
+ * scalars by value): C (m x n, ldc >= max(1, m)) = alpha * op(A) * op(B) + beta * C, where
+ * A is m x k (transa = 0, lda >= max(1, m)) or k x m (transa = 1, lda >= max(1, k)) and B
+ * is k x n (transb = 0, ldb >= max(1, k)) or n x k (transb = 1, ldb >= max(1, n)), all
+ * column-major. Computed as the row-major product C^T = op(B)^T op(A)^T (the swap trick
+ * of the same lecture, section 5.4). Returns 0, -i for the first illegal argument in this
+ * signature's order, or a cudaError_t. */
+int sgemm_f32_colmajor(int transa, int transb, int m, int n, int k, float alpha,
+                       const float *A, int lda, const float *B, int ldb, float beta, float *C,
+                       int ldc, cudaStream_t stream);
+
 /* Bytes of split-K workspace that sgemm_f32 would allocate for this problem on the
  * current device (0 when the chosen plan needs none). Host-only query. Returns the same
  * negative codes as sgemm_f32 for illegal shapes or leading dimensions, else 0. */

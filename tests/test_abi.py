@@ -79,7 +79,7 @@ def test_variant_table():
     for v in range(n):
         info = sg.sgemm_f32_variant_info(v)
         assert info["BM"] % 16 == 0 and info["BN"] % 16 == 0 and info["BK"] % 8 == 0
-        assert info["TM"] * info["TN"] >= 32 and info["threads"] % 32 == 0
+        assert info["TM"] * info["TN"] >= 16 and info["threads"] % 32 == 0
         # the CTA tile is exactly covered by its threads' accumulator tiles
         assert info["BM"] * info["BN"] == info["threads"] * info["TM"] * info["TN"]
     assert sg.sgemm_f32_variant_info(n) is None
@@ -138,3 +138,30 @@ def test_plan_split_never_exceeds_k_tiles():
         p = _plan(64, 64, K)
         info = sg.sgemm_f32_variant_info(p["variant"])
         assert 1 <= p["split"] <= -(-K // info["BK"])
+
+
+@pytest.mark.parametrize("args,code", [
+    ((2, 0, 4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -1),     # transa not 0/1
+    ((0, 5, 4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -2),     # transb not 0/1
+    ((0, 0, -1, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -3),    # M
+    ((1, 0, 4, 6, 5, 1.0, 8, 3, 8, 6, 0.0, 8, 6), -8),     # lda < M when A is transposed
+    ((0, 1, 4, 6, 5, 1.0, 8, 5, 8, 4, 0.0, 8, 6), -10),    # ldb < K when B is transposed
+    ((0, 0, 4, 6, 5, 1.0, 8, 5, 8, 6, 0.0, None, 6), -12),  # C missing
+    ((0, 0, 4, 6, 5, 1.0, 8, 5, 8, 6, 0.0, 8, 5), -13),    # ldc < N
+])
+def test_ex_argument_checks(args, code):
+    assert sg.sgemm_f32_ex(*args, stream=0) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, 0, -1, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -3),    # m
+    ((0, 0, 4, -1, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -4),    # n
+    ((0, 0, 4, 6, 5, 1.0, 8, 3, 8, 5, 0.0, 8, 4), -8),     # lda < m (A is m x k, col-major)
+    ((1, 0, 4, 6, 5, 1.0, 8, 4, 8, 5, 0.0, 8, 4), -8),     # lda < k when transposed
+    ((0, 0, 4, 6, 5, 1.0, 8, 4, 8, 4, 0.0, 8, 4), -10),    # ldb < k
+    ((0, 1, 4, 6, 5, 1.0, 8, 4, 8, 5, 0.0, 8, 4), -10),    # ldb < n when transposed
+    ((0, 0, 4, 6, 5, 1.0, 8, 4, 8, 5, 0.0, 8, 3), -13),    # ldc < m
+    ((0, 0, 4, 6, 5, 1.0, None, 4, 8, 5, 0.0, 8, 4), -7),  # A missing
+])
+def test_colmajor_argument_checks(args, code):
+    assert sg.sgemm_f32_colmajor(*args, stream=0) == code

@@ -15,7 +15,7 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 20  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 22  # compiled tile configurations; checked against the library below
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
