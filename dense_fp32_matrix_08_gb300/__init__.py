@@ -19,7 +19,7 @@ __all__ = [
     "LIB_PATH", "SgemmError", "lib", "sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced",
     "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
     "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex",
-    "sgemm_f32_colmajor", "sgemm_f32_3xtf32",
+    "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm", "EXPORTED",
 ]
 
@@ -27,6 +27,7 @@ __all__ = [
 EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspace_size",
             "sgemm_f32_plan", "sgemm_f32_num_variants", "sgemm_f32_variant_info",
             "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex", "sgemm_f32_colmajor",
+            "sgemv_f32", "sdot_f32",
             "sgemm_f32_3xtf32",
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status")
 
@@ -54,6 +55,8 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
     L.sgemm_f32_noalloc.argtypes = gemm + [vp]
     L.sgemm_f32_ex.argtypes = [i, i] + gemm + [vp]
+    L.sgemv_f32.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
+    L.sdot_f32.argtypes = [i, vp, i, vp, i, vp, vp]
     L.sgemm_f32_colmajor.argtypes = [i, i] + gemm + [vp]
     L.sgemm_f32_3xtf32.argtypes = gemm + [vp]
     L.sgemm_f32_3xtf32_workspace_size.argtypes = [i, i, i, psz]
@@ -135,6 +138,17 @@ def sgemm_f32_colmajor(transa, transb, m, n, k, alpha, A, lda, B, ldb, beta, C, 
     """Column-major BLAS-style sgemm (transa/transb: 0 = N, 1 = T)."""
     return lib.sgemm_f32_colmajor(int(transa), int(transb), m, n, k, alpha, _ptr(A), lda,
                                   _ptr(B), ldb, beta, _ptr(C), ldc, _stream(stream))
+
+
+def sgemv_f32(trans, M, N, alpha, A, lda, x, incx, beta, y, incy, stream=None) -> int:
+    """y = alpha op(A) x + beta y, A M x N row-major (trans: 0 = N, 1 = T)."""
+    return lib.sgemv_f32(int(trans), M, N, alpha, _ptr(A), lda, _ptr(x), incx, beta, _ptr(y),
+                         incy, _stream(stream))
+
+
+def sdot_f32(n, x, incx, y, incy, result, stream=None) -> int:
+    """*result (device) = sum x_i y_i."""
+    return lib.sdot_f32(n, _ptr(x), incx, _ptr(y), incy, _ptr(result), _stream(stream))
 
 
 def sgemm_f32_3xtf32(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

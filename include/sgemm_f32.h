@@ -104,6 +104,26 @@ int sgemm_f32_colmajor(int transa, int transb, int m, int n, int k, float alpha,
                        const float *A, int lda, const float *B, int ldb, float beta, float *C,
                        int ldc, cudaStream_t stream);
 
+/* y = alpha * op(A) * x + beta * y, the matrix-vector sibling of sgemm named with it in
+ * "Lecture 4 - GPU Acceleration", section 5.2 (cublasSgemv), for a row-major A (M x N,
+ * lda >= max(1, N)). trans = 0: y has M elements and x has N; trans = 1: op(A) = A^T, y has
+ * N elements and x has M. incx, incy: nonzero element strides (negative strides walk the
+ * vector backwards, as in BLAS). FP32 FMA accumulation in a fixed order (deterministic).
+ * alpha == 0 or an empty x: y = beta * y (y = 0 when beta == 0; x and A not read). Device
+ * pointers, asynchronous on `stream`; the transposed case takes a small workspace from the
+ * library's pool. Returns 0, -i for the first illegal argument (trans = 1, ..., incy = 11),
+ * or a cudaError_t. */
+int sgemv_f32(int trans, int M, int N, float alpha, const float *A, int lda, const float *x,
+              int incx, float beta, float *y, int incy, cudaStream_t stream);
+
+/* *result = sum_i x_i * y_i (cublasSdot, same lecture section), n elements with nonzero
+ * strides incx, incy; `result` is a device pointer written on `stream` (0 for n == 0). FP32
+ * FMA partial sums per block, added in a fixed order in a second launch (deterministic).
+ * Returns 0, -i for the first illegal argument (n = 1, ..., result = 6), or a
+ * cudaError_t. */
+int sdot_f32(int n, const float *x, int incx, const float *y, int incy, float *result,
+             cudaStream_t stream);
+
 /* Bytes of split-K workspace that sgemm_f32 would allocate for this problem on the
  * current device (0 when the chosen plan needs none). Host-only query. Returns the same
  * negative codes as sgemm_f32 for illegal shapes or leading dimensions, else 0. */

@@ -165,3 +165,26 @@ def test_ex_argument_checks(args, code):
 ])
 def test_colmajor_argument_checks(args, code):
     assert sg.sgemm_f32_colmajor(*args, stream=0) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((2, 4, 4, 1.0, 8, 4, 8, 1, 0.0, 8, 1), -1),
+    ((0, -1, 4, 1.0, 8, 4, 8, 1, 0.0, 8, 1), -2),
+    ((0, 4, -1, 1.0, 8, 4, 8, 1, 0.0, 8, 1), -3),
+    ((0, 4, 4, 1.0, None, 4, 8, 1, 0.0, 8, 1), -5),
+    ((0, 4, 4, 1.0, 8, 3, 8, 1, 0.0, 8, 1), -6),
+    ((0, 4, 4, 1.0, 8, 4, None, 1, 0.0, 8, 1), -7),
+    ((0, 4, 4, 1.0, 8, 4, 8, 0, 0.0, 8, 1), -8),
+    ((0, 4, 4, 1.0, 8, 4, 8, 1, 0.0, None, 1), -10),
+    ((0, 4, 4, 1.0, 8, 4, 8, 1, 0.0, 8, 0), -11),
+])
+def test_sgemv_argument_checks(args, code):
+    assert sg.sgemv_f32(*args, stream=0) == code
+
+
+@pytest.mark.parametrize("args,code", [
+    ((-1, 8, 1, 8, 1, 8), -1), ((4, None, 1, 8, 1, 8), -2), ((4, 8, 0, 8, 1, 8), -3),
+    ((4, 8, 1, None, 1, 8), -4), ((4, 8, 1, 8, 0, 8), -5), ((4, 8, 1, 8, 1, None), -6),
+])
+def test_sdot_argument_checks(args, code):
+    assert sg.sdot_f32(*args, stream=0) == code
