@@ -19,7 +19,7 @@ __all__ = [
     "LIB_PATH", "SgemmError", "lib", "sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced",
     "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
     "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex",
-    "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_3xtf32",
+    "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_status", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm", "EXPORTED",
 ]
 
@@ -27,7 +27,7 @@ __all__ = [
 EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspace_size",
             "sgemm_f32_plan", "sgemm_f32_num_variants", "sgemm_f32_variant_info",
             "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex", "sgemm_f32_colmajor",
-            "sgemv_f32", "sdot_f32",
+            "sgemv_f32", "sdot_f32", "sgemm_f32_status",
             "sgemm_f32_3xtf32",
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status")
 
@@ -61,6 +61,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_3xtf32.argtypes = gemm + [vp]
     L.sgemm_f32_3xtf32_workspace_size.argtypes = [i, i, i, psz]
     L.sgemm_f32_3xtf32_status.argtypes = [pi]
+    L.sgemm_f32_status.argtypes = [pi]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
@@ -161,6 +162,13 @@ def sgemm_f32_3xtf32_workspace_size(M, N, K) -> tuple[int, int]:
     b = ctypes.c_size_t(0)
     rc = lib.sgemm_f32_3xtf32_workspace_size(M, N, K, ctypes.byref(b))
     return rc, b.value
+
+
+def sgemm_f32_status() -> tuple[int, int]:
+    """(call status, device status word of the TMA-fed FFMA kernel); reading clears it."""
+    v = ctypes.c_int(0)
+    rc = lib.sgemm_f32_status(ctypes.byref(v))
+    return rc, v.value
 
 
 def sgemm_f32_3xtf32_status() -> tuple[int, int]:

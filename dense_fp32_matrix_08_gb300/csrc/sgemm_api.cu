@@ -11,6 +11,7 @@
 
 #include "../../include/sgemm_f32.h"
 #include "sgemm_aux.cuh"
+#include "sgemm_ffma_tma.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_plan.h"
 #include "sgemm_variants.cuh"
@@ -21,7 +22,12 @@ static const VariantKernels kKernels[kNumVariants] = {
 #define SGEMM_KERNELS_ENTRY(v) variant_kernels<v>(),
     SGEMM_FOR_EACH_VARIANT(SGEMM_KERNELS_ENTRY)
 #undef SGEMM_KERNELS_ENTRY
+    VariantKernels{},  // kTmaVariant: launched through run_tma
 };
+static_assert(kTmaVariant == kNumVariants - 1, "the TMA variant is the last table entry");
+
+// Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
+__device__ int g_ffma_status;
 
 // ------------------------------------------------------------------------------------
 // Per-device one-time setup: opt every kernel into its dynamic shared memory and cache
@@ -30,6 +36,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   std::once_flag once;
   int num_sms = 0;
+  int *status = nullptr;  // device address of g_ffma_status
   cudaMemPool_t pool = nullptr;  // split-K workspace pool of this device
   cudaError_t err = cudaSuccess;
 };
@@ -51,6 +58,11 @@ cudaError_t device_setup(int *num_sms) {
             err = cudaFuncSetAttribute(kKernels[v].k[a][b],
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kKernels[v].smem);
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(tma::sgemm_tma_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tma::SMEM_BYTES);
+    if (err == cudaSuccess)
+      err = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_ffma_status);
     // A pool of the library's own for split-K workspaces. It keeps freed memory (release
     // threshold: never), so a stream-ordered allocation of a recently freed size is a
     // cheap reuse instead of a fresh mapping; the default pool returns its memory at every
@@ -81,7 +93,7 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
                         int force_split) {
   struct Entry {
     int M, N, K, num_sms, force_v, force_split;
-    unsigned flags;  // alpha == 0, beta != 0, beta == 1, op(A) transposed, op(B) transposed
+    unsigned flags;  // alpha == 0, beta != 0, beta == 1, op(A) / op(B) transposed, TMA-able
     bool valid;
     Plan plan;
   };
@@ -90,7 +102,7 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   thread_local int next = 0;
   const unsigned flags = (alpha == 0.0f ? 1u : 0u) | (beta != 0.0f ? 2u : 0u) |
                          (beta == 1.0f ? 4u : 0u) | (pr.transa ? 8u : 0u) |
-                         (pr.transb ? 16u : 0u);
+                         (pr.transb ? 16u : 0u) | (pr.tma_ok ? 32u : 0u);
   for (int i = 0; i < kEntries; ++i) {
     const Entry &e = cache[i];
     if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
@@ -102,6 +114,12 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   e = Entry{pr.M, pr.N, pr.K, num_sms, force_v, force_split, flags, true,
             make_plan(pr, alpha, beta, num_sms, force_v, force_split)};
   return e.plan;
+}
+
+static int *status_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_dev[dev].status;
 }
 
 cudaMemPool_t workspace_pool() {
@@ -153,6 +171,15 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   p.tiles_n = pl.tiles_n;
   p.group_m = pl.group_m;
   p.vec_c = vec_c ? 1 : 0;
+  if (vs.tma) {
+    CUtensorMap map_a, map_b;
+    if (!encode_map_2d(&map_a, A, pr.M, pr.K, pr.lda, tma::BK, tma::BM, true) ||
+        !encode_map_2d(&map_b, B, pr.K, pr.N, pr.ldb, tma::BN, tma::BK, false))
+      return (int)cudaErrorInvalidValue;
+    if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
+    tma::sgemm_tma_kernel<<<pl.ctas, tma::THREADS, tma::SMEM_BYTES, stream>>>(map_a, map_b, p,
+                                                                             status_word());
+  } else {
   const int apath = !pr.transa ? APATH_N
                     : ((pr.lda % 4 == 0) && aligned16(A)) ? APATH_T16 : APATH_T4;
   const int bpath = pr.transb ? BPATH_T
@@ -161,6 +188,7 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   if (fn == nullptr) return kErrBadVariant;  // forced variant without transposed paths
   if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
   fn<<<pl.ctas, vs.threads, vs.smem_bytes, stream>>>(p);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   const long long tail_tiles = (long long)pl.tiles_m * pl.tiles_n - pl.main_tiles;
@@ -181,11 +209,14 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
                        int force_split, int ws_mode, void *ws, size_t ws_bytes,
                        cudaStream_t stream, int transa = 0, int transb = 0) {
   Problem pr{M, N, K, lda, ldb, ldc, transa, transb};
+  pr.tma_ok = !transa && !transb && lda % 4 == 0 && ldb % 4 == 0 && aligned16(A) &&
+              aligned16(B) && A != nullptr && B != nullptr;
   int rc = (transa || transb) ? validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr)
                               : validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
   if (rc != 0) return rc;
   if (M == 0 || N == 0) return 0;
   if (force_v >= kNumVariants || force_v < -1) return kErrBadVariant;
+  if (force_v >= 0 && kVariants[force_v].tma && !pr.tma_ok) return kErrBadVariant;
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
@@ -270,6 +301,7 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
                    int num_sms, int *variant, int *split, int *main_tiles, int *launches,
                    size_t *ws_bytes) {
   Problem pr{M, N, K, lda, ldb, ldc};
+  pr.tma_ok = lda % 4 == 0 && ldb % 4 == 0;  // pointers assumed 16-byte aligned
   int rc = validate(pr, alpha, true, true, true);
   if (rc != 0) return rc;
   if (num_sms <= 0) {
@@ -307,5 +339,15 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
 }
 
 const char *sgemm_f32_version(void) { return "sgemm_f32 0.1.0 sm_103a"; }
+
+int sgemm_f32_status(int *status) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_ffma_status, sizeof(int));
+  if (e != cudaSuccess) return (int)e;
+  const int zero = 0;
+  e = cudaMemcpyToSymbol(g_ffma_status, &zero, sizeof(int));
+  if (status) *status = v;
+  return (int)e;
+}
 
 }  // extern "C"

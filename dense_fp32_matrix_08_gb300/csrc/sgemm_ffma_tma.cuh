@@ -1,0 +1,226 @@
+// TMA-fed FP32 FFMA2 GEMM for sm_103a: C = alpha * A * B + beta * C, row-major, for
+// 16-byte aligned A and B with lda, ldb multiples of 4 and no transposition.
+//
+// Same register outer product as sgemm_ffma.cuh (8 x 16 FFMA2 thread tiles in 64 x 64 warp
+// tiles, four warps per 128 x 128 CTA tile, two CTAs per SM), but the operand tiles reach
+// shared memory by TMA instead of per-thread copies: one thread issues two cp.async.bulk.
+// tensor copies per 32-wide K block into a 3-stage ring, and the math warps spend no issue
+// slots on address arithmetic or copies (on this GPU those took about 18% of the slots of
+// the copy-based kernel). Each stage has a "full" mbarrier (TMA bytes) and an "empty"
+// mbarrier (one arrival per warp when it has finished reading the stage).
+//
+// Layouts in shared memory:
+//  * A tile: 128 rows (m) x 32 k, as stored (k contiguous), written by TMA with the 128-byte
+//    swizzle: the 16-byte chunk c of row r sits at chunk c ^ (r & 7). A thread's eight rows
+//    are r = lane_m + 8 i, so the eight row groups of a warp hit eight different chunks:
+//    every 128-bit fragment load is conflict-free. One float4 gives a row's values for 4
+//    consecutive k, so A fragments are loaded once per 4 k steps.
+//  * B tile: 32 k x 128 n, as stored (n contiguous), no swizzle; a thread's 16 columns are
+//    four float4 at stride 16 columns, as in the copy-based kernel.
+// Ragged edges: TMA fills out-of-range rows / columns / k with zeros, so the main loop has
+// no masks; the epilogue masks rows and columns. Every mbarrier wait is bounded; a wait
+// that gives up sets a device status word and the CTA stops computing (the result is then
+// invalid, which the status reports).
+#pragma once
+
+#include <cuda.h>
+
+#include "sgemm_ffma.cuh"
+#include "sgemm_ptx.cuh"
+
+namespace sgemm {
+namespace tma {
+
+constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3, THREADS = 128;
+constexpr int WM = 64, WN = 64, TM = 8, TN = 16, LM = 8, LN = 4, WARPS_N = 2;
+constexpr int A_BYTES = BM * BK * 4, B_BYTES = BK * BN * 4;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 64;  // + alignment slack, barriers
+
+static_assert(LM * LN == 32 && WM == LM * TM && WN == LN * TN, "lane layout");
+static_assert((BM / WM) * (BN / WN) * 32 == THREADS, "four warps");
+static_assert(BK * 4 == 128, "A rows are one 128-byte swizzle span");
+
+__global__ void __launch_bounds__(THREADS, 2)
+    sgemm_tma_kernel(const __grid_constant__ CUtensorMap map_a,
+                     const __grid_constant__ CUtensorMap map_b, const GemmParams p,
+                     int *status) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = saddr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
+  const float *smem_f = reinterpret_cast<const float *>(smem_raw + (base - raw));
+  const uint32_t bars = base + STAGES * STAGE_BYTES;  // full[s] at 8 s, empty[s] at 8 (S + s)
+
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  const int warp = tid >> 5;
+  const int warp_m = warp / WARPS_N;
+  const int warp_n = warp % WARPS_N;
+  // 2 x 2 lane groups (see sgemm_ffma.cuh): both fragment loads take 2 wavefronts
+  const int lane_hi = lane >> 2;
+  const int lane_n = (lane_hi % (LN / 2)) * 2 + (lane & 1);
+  const int lane_m = (lane_hi / (LN / 2)) * 2 + ((lane >> 1) & 1);
+
+  // work decomposition: whole tiles, then K slices of the remaining tiles (GemmParams)
+  const int w = blockIdx.x;
+  const bool partial = w >= p.main_tiles;
+  int tile = w, k_begin = 0, k_end = p.K;
+  if (partial) {
+    const int u = w - p.main_tiles;
+    tile = p.main_tiles + u / p.split;
+    k_begin = (u % p.split) * p.k_per_split;  // a multiple of BK
+    k_end = min(p.K, k_begin + p.k_per_split);
+  }
+  int tm, tn;
+  tile_coords(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+  const int m0 = tm * BM;
+  const int n0 = tn * BN;
+  const int KT = (k_end - k_begin + BK - 1) / BK;
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bars + 8 * s, 1);
+      mbar_init(bars + 8 * (STAGES + s), THREADS / 32);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  auto issue = [&](int kt) {  // thread 0 only
+    const int s = kt % STAGES;
+    const uint32_t full = bars + 8 * s;
+    const uint32_t st = base + s * STAGE_BYTES;
+    mbar_expect_tx(full, STAGE_BYTES);
+    tma_load_2d(st, &map_a, k_begin + kt * BK, m0, full);
+    tma_load_2d(st + A_BYTES, &map_b, n0, k_begin + kt * BK, full);
+  };
+  int issued = 0;
+  if (tid == 0) {
+    tma_prefetch_map(&map_a);
+    tma_prefetch_map(&map_b);
+    for (int kt = 0; kt < STAGES - 1 && kt < KT; ++kt) issue(kt);
+    issued = min(STAGES - 1, KT);
+  }
+
+  unsigned long long acc[TM][TN / 2];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0;
+
+  const int a_row = warp_m * WM + lane_m;        // + 8 i
+  const int swz = lane_m & 7;                    // == a_row & 7 for every i
+  const int b_col0 = warp_n * WN + lane_n * 4;   // + 16 jj
+  bool ok = true;
+
+  for (int kt = 0; kt < KT; ++kt) {
+    const int s = kt % STAGES;
+    if (!mbar_wait(bars + 8 * s, (uint32_t)(kt / STAGES) & 1u)) {
+      ok = false;
+      if (lane == 0) atomicCAS(status, 0, 1);
+      break;
+    }
+    const float *as = smem_f + s * (STAGE_BYTES / 4);
+    const float *bs = as + A_BYTES / 4;
+#pragma unroll 1
+    for (int c = 0; c < BK / 4; ++c) {
+      float4 fa[TM];
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+        fa[i] = *reinterpret_cast<const float4 *>(as + (a_row + 8 * i) * BK + ((c ^ swz) << 2));
+      float4 fb[2][TN / 4];
+#pragma unroll
+      for (int jj = 0; jj < TN / 4; ++jj)
+        fb[0][jj] = *reinterpret_cast<const float4 *>(bs + (4 * c) * BN + b_col0 + 16 * jj);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int cur = kk & 1;
+        if (kk + 1 < 4) {
+#pragma unroll
+          for (int jj = 0; jj < TN / 4; ++jj)
+            fb[cur ^ 1][jj] =
+                *reinterpret_cast<const float4 *>(bs + (4 * c + kk + 1) * BN + b_col0 + 16 * jj);
+        }
+        unsigned long long b2[TN / 2];
+#pragma unroll
+        for (int jj = 0; jj < TN / 4; ++jj) {
+          b2[2 * jj] = pack2(fb[cur][jj].x, fb[cur][jj].y);
+          b2[2 * jj + 1] = pack2(fb[cur][jj].z, fb[cur][jj].w);
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+          const float a = kk == 0 ? fa[i].x : kk == 1 ? fa[i].y : kk == 2 ? fa[i].z : fa[i].w;
+          const unsigned long long a2 = pack2(a, a);
+#pragma unroll
+          for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], a2, b2[j]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // this warp is done with stage s
+    if (tid == 0 && issued < KT) {
+      // refill the stage that k tile kt - 1 used (kt + STAGES - 1 lands there)
+      if (kt >= 1 && !mbar_wait(bars + 8 * (STAGES + (kt - 1) % STAGES),
+                                (uint32_t)((kt - 1) / STAGES) & 1u)) {
+        atomicCAS(status, 0, 2);
+      } else {
+        issue(issued);
+        ++issued;
+      }
+    }
+  }
+  // Thread 0 may not leave while copies it issued are in flight: wait for the last ones.
+  if (tid == 0) {
+    for (int kt = issued - 1; kt >= 0 && kt >= issued - STAGES; --kt)
+      mbar_wait(bars + 8 * (kt % STAGES), (uint32_t)(kt / STAGES) & 1u);
+  }
+  if (!ok) return;
+
+  // ---- epilogue: thread element (i, 4 jj + e) is row a_row + 8 i, column b_col0 + 16 jj + e
+  if (partial) {
+    float *wt = p.ws + (long long)(w - p.main_tiles) * (BM * BN);
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+      for (int jj = 0; jj < TN / 4; ++jj) {
+        const float2 lo = unpack2(acc[i][2 * jj]), hi = unpack2(acc[i][2 * jj + 1]);
+        *reinterpret_cast<float4 *>(wt + (a_row + 8 * i) * BN + b_col0 + 16 * jj) =
+            make_float4(lo.x, lo.y, hi.x, hi.y);
+      }
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int row = m0 + a_row + 8 * i;
+    if (row >= p.M) continue;
+#pragma unroll
+    for (int jj = 0; jj < TN / 4; ++jj) {
+      const int col = n0 + b_col0 + 16 * jj;
+      if (col >= p.N) continue;
+      const float2 lo = unpack2(acc[i][2 * jj]), hi = unpack2(acc[i][2 * jj + 1]);
+      const float v[4] = {lo.x, lo.y, hi.x, hi.y};
+      float *dst = p.C + (long long)row * p.ldc + col;
+      if (p.vec_c && col + 3 < p.N) {
+        float4 out;
+        if (p.beta != 0.0f) {
+          const float4 old = *reinterpret_cast<const float4 *>(dst);
+          out.x = fmaf(p.alpha, v[0], p.beta * old.x);
+          out.y = fmaf(p.alpha, v[1], p.beta * old.y);
+          out.z = fmaf(p.alpha, v[2], p.beta * old.z);
+          out.w = fmaf(p.alpha, v[3], p.beta * old.w);
+        } else {
+          out = make_float4(p.alpha * v[0], p.alpha * v[1], p.alpha * v[2], p.alpha * v[3]);
+        }
+        *reinterpret_cast<float4 *>(dst) = out;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (col + e < p.N)
+            dst[e] = (p.beta != 0.0f) ? fmaf(p.alpha, v[e], p.beta * dst[e]) : p.alpha * v[e];
+      }
+    }
+  }
+}
+
+}  // namespace tma
+}  // namespace sgemm

@@ -16,6 +16,7 @@ constexpr int kErrBadVariant = -14;
 struct Problem {
   int M, N, K, lda, ldb, ldc;
   int transa = 0, transb = 0;  // 1: op(X) = X_st^T (see sgemm_f32_ex)
+  bool tma_ok = false;         // A, B 16-byte aligned with lda, ldb % 4 == 0 (TMA-fed kernel)
 };
 
 // Shape of one compiled tile configuration (mirrors TileConfig in sgemm_ffma.cuh).
@@ -24,6 +25,7 @@ struct VariantShape {
   double eff;  // modelled fraction of the FP32 pipe this configuration sustains
   bool automatic;  // considered by the automatic plan (others only when forced)
   bool trans_ok;   // compiled with the transposed-operand copy paths
+  bool tma = false;  // the TMA-fed kernel (sgemm_ffma_tma.cuh), aligned row-major operands only
 };
 
 // mode: 0 scalar FFMA, 1 FFMA2 with register broadcast, 2 FFMA2 with duplicated A in smem
@@ -54,8 +56,16 @@ constexpr VariantShape kVariants[] = {
     {128, 128, 16, 128, 4, 32, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.80, false, false},
     {16, 512, 16, 128, 8, 8, 3, 2, 1, smem_of(16, 512, 16, 3, 1), 0.60, false, false},
     {128, 16, 32, 128, 4, 4, 4, 3, 0, smem_of(128, 16, 32, 4, 0), 0.50, false, false},
+    {128, 128, 16, 128, 8, 16, 4, 2, 1, smem_of(128, 128, 16, 4, 1), 0.80, false, false},
+    {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 0.80, false, false},
+    {128, 128, 8, 128, 8, 16, 6, 2, 1, smem_of(128, 128, 8, 6, 1), 0.80, false, false},
+    {128, 128, 16, 128, 8, 16, 3, 2, 2, smem_of(128, 128, 16, 3, 2), 0.80, false, false},
+    // 26: TMA-fed 128 x 128 x 32, 3 stages, 2 CTAs/SM (its own kernel, see kTmaVariant)
+    {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 0.96, true, false, true},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
+constexpr int kTmaVariant = 26;
+static_assert(kVariants[kTmaVariant].tma, "TMA variant index");
 
 struct Plan {
   int variant = -1;     // -1: no GEMM kernel (beta-scale only, or nothing)
@@ -227,6 +237,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   for (int v = v_lo; v <= v_hi; ++v) {
     if (force_v < 0 && !kVariants[v].automatic) continue;
     if (trans && !kVariants[v].trans_ok) continue;
+    if (kVariants[v].tma && !p.tma_ok) continue;
     const VariantShape &s = kVariants[v];
     const long long tiles = ceil_div(p.M, s.BM) * ceil_div(p.N, s.BN);
     const long long kt = ceil_div(p.K, s.BK);

@@ -43,10 +43,14 @@ template <> struct VariantCfg<18> { using type = TileConfig<128, 256, 16, 32, 12
 template <> struct VariantCfg<19> { using type = TileConfig<128, 128, 16, 32, 128, 4, 32, 3, 2, 1>; };
 template <> struct VariantCfg<20> { using type = TileConfig<16, 512, 16, 16, 128, 8, 8, 3, 2, 1>; };
 template <> struct VariantCfg<21> { using type = TileConfig<128, 16, 32, 32, 16, 4, 4, 4, 3, 0>; };
+template <> struct VariantCfg<22> { using type = TileConfig<128, 128, 16, 64, 64, 8, 16, 4, 2, 1>; };
+template <> struct VariantCfg<23> { using type = TileConfig<128, 128, 32, 64, 64, 8, 16, 3, 2, 1>; };
+template <> struct VariantCfg<24> { using type = TileConfig<128, 128, 8, 64, 64, 8, 16, 6, 2, 1>; };
+template <> struct VariantCfg<25> { using type = TileConfig<128, 128, 16, 64, 64, 8, 16, 3, 2, 2>; };
 
 #define SGEMM_FOR_EACH_VARIANT(X) \
   X(0) X(1) X(2) X(3) X(4) X(5) X(6) X(7) X(8) X(9) X(10) X(11) X(12) X(13) X(14) X(15) \
-  X(16) X(17) X(18) X(19) X(20) X(21)
+  X(16) X(17) X(18) X(19) X(20) X(21) X(22) X(23) X(24) X(25)
 
 template <class Cfg>
 constexpr bool matches(const VariantShape &s) {

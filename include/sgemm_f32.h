@@ -139,6 +139,7 @@ int sgemm_f32_ws(int M, int N, int K, float alpha, const float *A, int lda, cons
 
 /* Launch plan chosen for a problem, for tests and tuning. Host-only: no CUDA call is made
  * when num_sms > 0 (the SM count to plan for); num_sms == 0 asks the current device.
+ * A and B are assumed 16-byte aligned (they decide whether the TMA-fed kernel applies).
  * alpha and beta matter only through their special values (alpha == 0, beta == 0, 1).
  * Outputs (any may be NULL):
  *   variant  tile configuration index (0 .. sgemm_f32_num_variants() - 1), -1 when no
@@ -167,7 +168,8 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
  * (1: no split-K); -1 computes the full waves of tiles whole and splits only the tiles of
  * the last, partial wave (slice count chosen to fill it); <= -2 does the same with
  * -split slices; 0 is automatic. Slice counts are clamped so that every slice holds at
- * least one K tile. Returns -14 for an out-of-range variant. */
+ * least one K tile. Returns -14 for an out-of-range variant, or for the TMA-fed
+ * configuration when A or B is not 16-byte aligned with lda, ldb multiples of 4. */
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);
@@ -232,6 +234,12 @@ int sgemm_f32_3xtf32_workspace_size(int M, int N, int K, size_t *bytes);
  * legacy stream): 0 = fine; 1, 2, 3 = a bounded wait of the producer, MMA or epilogue
  * threads gave up (the kernel then skipped work and the result is not valid). */
 int sgemm_f32_3xtf32_status(int *status);
+
+/* Reads and clears the device status word of the TMA-fed FFMA kernel (synchronising copy
+ * on the legacy stream): 0 = fine; 1 or 2 = a bounded mbarrier wait gave up (a consumer
+ * waiting for data, or the producer waiting for a free stage), in which case the kernel
+ * stopped computing and the result of that call is not valid. */
+int sgemm_f32_status(int *status);
 
 /* Library version string, e.g. "sgemm_f32 0.1.0 sm_103a". */
 const char *sgemm_f32_version(void);

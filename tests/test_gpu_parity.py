@@ -15,7 +15,8 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 22  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 27  # compiled tile configurations; checked against the library below
+TMA_VARIANT = 26   # the TMA-fed kernel (aligned, row-major operands only)
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -105,9 +106,13 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
+    if not aligned and variant == TMA_VARIANT:
+        pytest.skip("the TMA-fed configuration needs aligned operands")
     for (M, N, K) in RAGGED:
         A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
-        if aligned:
+        if aligned and variant == TMA_VARIANT:  # TMA needs ld % 4 == 0: pad the rows
+            lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
+        elif aligned:
             lds, offs = (None, None, None), (0, 0, 0)
         else:  # odd leading dimensions and odd element offsets: 32-bit paths everywhere
             lds, offs = (K + 1, N + 3, N + 5), (1, 3, 5)
@@ -151,6 +156,20 @@ def test_variant_count():
     assert sg.sgemm_f32_num_variants() == NUM_VARIANTS
 
 
+def test_tma_variant_refuses_unaligned():
+    A, B, C = make_inputs(64, 64, 64, seed=12)
+    dA, _ = to_device_view(A, 65, 1)
+    dB, _ = to_device_view(B)
+    dC, _ = to_device_view(C)
+    assert sg.sgemm_f32_forced(64, 64, 64, 1.0, dA, 65, dB, 64, 0.0, dC, 64, TMA_VARIANT, 1) == -14
+
+
+def test_status_words_clear():
+    A, B, C = make_inputs(300, 300, 300, seed=13)
+    out, _ = _run(A, B, C, 1.0, 0.5, variant=TMA_VARIANT, split=1)
+    assert sg.sgemm_f32_status() == (0, 0)
+
+
 def test_beta_zero_does_not_read_c():
     A, B, _ = make_inputs(70, 90, 33, seed=5)
     C = torch.full((70, 90), float("nan"))
@@ -192,7 +211,7 @@ def test_fp32_fidelity_exact():
     A = torch.full((M, K), 1.0 + 2.0 ** -15)
     B = torch.ones((K, N))
     C = torch.zeros((M, N))
-    for v in _variants():
+    for v in _variants():  # packed 64 x 256 and 256 x 64 operands: TMA-able as well
         out, _ = _run(A, B, C, 1.0, 0.0, variant=v, split=1)
         assert torch.all(out == 256.0 + 2.0 ** -7), f"variant {v}"
 
