@@ -20,7 +20,8 @@ __all__ = [
     "sgemm_f32_workspace_size", "sgemm_f32_plan", "sgemm_f32_num_variants",
     "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex",
     "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_status", "sgemm_f32_3xtf32",
-    "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm", "EXPORTED",
+    "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
+    "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -29,7 +30,8 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex", "sgemm_f32_colmajor",
             "sgemv_f32", "sdot_f32", "sgemm_f32_status",
             "sgemm_f32_3xtf32",
-            "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status")
+            "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status",
+            "sgemm_f32_ex_forced")
 
 
 class SgemmError(RuntimeError):
@@ -55,6 +57,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_forced.argtypes = gemm + [i, i, vp]
     L.sgemm_f32_noalloc.argtypes = gemm + [vp]
     L.sgemm_f32_ex.argtypes = [i, i] + gemm + [vp]
+    L.sgemm_f32_ex_forced.argtypes = [i, i] + gemm + [i, i, vp]
     L.sgemv_f32.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     L.sdot_f32.argtypes = [i, vp, i, vp, i, vp, vp]
     L.sgemm_f32_colmajor.argtypes = [i, i] + gemm + [vp]
@@ -117,6 +120,14 @@ def sgemm_f32_forced(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant, spli
                      stream=None) -> int:
     return lib.sgemm_f32_forced(M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C),
                                 ldc, variant, split, _stream(stream))
+
+
+def sgemm_f32_ex_forced(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant,
+                        split, stream=None) -> int:
+    """sgemm_f32_ex with the tile configuration and split-K layout forced."""
+    return lib.sgemm_f32_ex_forced(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda,
+                                   _ptr(B), ldb, beta, _ptr(C), ldc, variant, split,
+                                   _stream(stream))
 
 
 def sgemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

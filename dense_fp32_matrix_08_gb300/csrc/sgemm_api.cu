@@ -7,11 +7,12 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <limits>
 #include <mutex>
 
 #include "../../include/sgemm_f32.h"
 #include "sgemm_aux.cuh"
-#include "sgemm_ffma_tma.cuh"
+#include "sgemm_ffma_kpair.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_plan.h"
 #include "sgemm_variants.cuh"
@@ -22,9 +23,16 @@ static const VariantKernels kKernels[kNumVariants] = {
 #define SGEMM_KERNELS_ENTRY(v) variant_kernels<v>(),
     SGEMM_FOR_EACH_VARIANT(SGEMM_KERNELS_ENTRY)
 #undef SGEMM_KERNELS_ENTRY
-    VariantKernels{},  // kTmaVariant: launched through run_tma
+    VariantKernels{},  // kTmaVariant: its own kernel (sgemm_tma.cu)
+    VariantKernels{},  // K-paired variants: their own kernel (sgemm_kpair.cu)
+    VariantKernels{},
+    VariantKernels{},
+    VariantKernels{},  // more TMA-fed instances (sgemm_tma.cu)
+    VariantKernels{},
+    VariantKernels{},
 };
-static_assert(kTmaVariant == kNumVariants - 1, "the TMA variant is the last table entry");
+static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kNumVariants == 33,
+              "the generic variants come first, then the TMA-fed ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
 __device__ int g_ffma_status;
@@ -58,9 +66,8 @@ cudaError_t device_setup(int *num_sms) {
             err = cudaFuncSetAttribute(kKernels[v].k[a][b],
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kKernels[v].smem);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(tma::sgemm_tma_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, tma::SMEM_BYTES);
+    if (err == cudaSuccess) err = tma_setup();
+    if (err == cudaSuccess) err = kpair_setup();
     if (err == cudaSuccess)
       err = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_ffma_status);
     // A pool of the library's own for split-K workspaces. It keeps freed memory (release
@@ -102,7 +109,8 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   thread_local int next = 0;
   const unsigned flags = (alpha == 0.0f ? 1u : 0u) | (beta != 0.0f ? 2u : 0u) |
                          (beta == 1.0f ? 4u : 0u) | (pr.transa ? 8u : 0u) |
-                         (pr.transb ? 16u : 0u) | (pr.tma_ok ? 32u : 0u);
+                         (pr.transb ? 16u : 0u) | (pr.tma_ok ? 32u : 0u) |
+                         (pr.kpair_ok ? 64u : 0u) | (pr.b_kmajor ? 128u : 0u);
   for (int i = 0; i < kEntries; ++i) {
     const Entry &e = cache[i];
     if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
@@ -171,14 +179,29 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   p.tiles_n = pl.tiles_n;
   p.group_m = pl.group_m;
   p.vec_c = vec_c ? 1 : 0;
-  if (vs.tma) {
-    CUtensorMap map_a, map_b;
-    if (!encode_map_2d(&map_a, A, pr.M, pr.K, pr.lda, tma::BK, tma::BM, true) ||
-        !encode_map_2d(&map_b, B, pr.K, pr.N, pr.ldb, tma::BN, tma::BK, false))
+  if (vs.kpair) {
+    const float *Bt = B;
+    long long ldbt = pr.ldb;
+    if (pl.bt_bytes > 0) {  // row-major B: copy it to B^T (N x K) at the front of ws
+      float *bt = ws;
+      p.ws = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + pl.bt_bytes);
+      cudaError_t te = launch_transpose_b(B, pr.ldb, pr.K, pr.N, bt, pl.ldbt, num_sms, stream);
+      if (te != cudaSuccess) return (int)te;
+      Bt = bt;
+      ldbt = pl.ldbt;
+    }
+    ws = p.ws;
+    CUtensorMap map_a, map_bt;
+    if (!encode_map_2d(&map_a, A, pr.M, pr.K, pr.lda, kpair::BK, kpair::BM, true) ||
+        !encode_map_2d(&map_bt, Bt, pr.N, pr.K, ldbt, kpair::BK, kpair::BN, true))
       return (int)cudaErrorInvalidValue;
     if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
-    tma::sgemm_tma_kernel<<<pl.ctas, tma::THREADS, tma::SMEM_BYTES, stream>>>(map_a, map_b, p,
-                                                                             status_word());
+    cudaError_t ke = launch_kpair(vs.stages, map_a, map_bt, p, pl.ctas, status_word(), stream);
+    if (ke != cudaSuccess) return (int)ke;
+  } else if (vs.tma) {
+    if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
+    cudaError_t ke = launch_tma(vs.inst, A, pr.lda, B, pr.ldb, p, pl.ctas, status_word(), stream);
+    if (ke != cudaSuccess) return (int)ke;
   } else {
   const int apath = !pr.transa ? APATH_N
                     : ((pr.lda % 4 == 0) && aligned16(A)) ? APATH_T16 : APATH_T4;
@@ -211,16 +234,22 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   Problem pr{M, N, K, lda, ldb, ldc, transa, transb};
   pr.tma_ok = !transa && !transb && lda % 4 == 0 && ldb % 4 == 0 && aligned16(A) &&
               aligned16(B) && A != nullptr && B != nullptr;
+  pr.kpair_ok = !transa && lda % 4 == 0 && aligned16(A) && A != nullptr && B != nullptr;
+  pr.b_kmajor = transb && ldb % 4 == 0 && aligned16(B);
   int rc = (transa || transb) ? validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr)
                               : validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
   if (rc != 0) return rc;
   if (M == 0 || N == 0) return 0;
   if (force_v >= kNumVariants || force_v < -1) return kErrBadVariant;
   if (force_v >= 0 && kVariants[force_v].tma && !pr.tma_ok) return kErrBadVariant;
+  if (force_v >= 0 && kVariants[force_v].kpair && !pr.kpair_ok) return kErrBadVariant;
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
   Plan pl = cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
+  // No candidate fitted (a forced configuration whose workspace exceeds the limits).
+  if (pl.variant < 0 && alpha != 0.0f && K > 0) return force_v >= 0 ? kErrBadVariant
+                                                                    : kErrWorkspace;
   float *wsp = nullptr;
   if (pl.ws_bytes > 0) {
     if (ws_mode == 1) {
@@ -291,6 +320,19 @@ int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      nullptr, 0, stream);
 }
 
+int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha,
+                        const float *A, int lda, const float *B, int ldb, float beta, float *C,
+                        int ldc, int variant, int split, cudaStream_t stream) {
+  Problem pr{M, N, K, lda, ldb, ldc, transa, transb};
+  const int rc = validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
+  if (rc != 0) return rc;
+  if (variant >= 0 && variant < kNumVariants && (transa || transb) &&
+      !kVariants[variant].trans_ok)
+    return kErrBadVariant;
+  return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant, split, 0, nullptr,
+                     0, stream, transa, transb);
+}
+
 int sgemm_f32_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
                              size_t *bytes) {
   return sgemm_f32_plan(M, N, K, lda, ldb, ldc, 1.0f, 1.0f, 0, nullptr, nullptr, nullptr,
@@ -302,6 +344,7 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
                    size_t *ws_bytes) {
   Problem pr{M, N, K, lda, ldb, ldc};
   pr.tma_ok = lda % 4 == 0 && ldb % 4 == 0;  // pointers assumed 16-byte aligned
+  pr.kpair_ok = lda % 4 == 0;
   int rc = validate(pr, alpha, true, true, true);
   if (rc != 0) return rc;
   if (num_sms <= 0) {

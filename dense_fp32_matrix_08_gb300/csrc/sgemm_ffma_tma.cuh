@@ -1,13 +1,15 @@
 // TMA-fed FP32 FFMA2 GEMM for sm_103a: C = alpha * A * B + beta * C, row-major, for
 // 16-byte aligned A and B with lda, ldb multiples of 4 and no transposition.
 //
-// Same register outer product as sgemm_ffma.cuh (8 x 16 FFMA2 thread tiles in 64 x 64 warp
-// tiles, four warps per 128 x 128 CTA tile, two CTAs per SM), but the operand tiles reach
-// shared memory by TMA instead of per-thread copies: one thread issues two cp.async.bulk.
-// tensor copies per 32-wide K block into a 3-stage ring, and the math warps spend no issue
-// slots on address arithmetic or copies (on this GPU those took about 18% of the slots of
-// the copy-based kernel). Each stage has a "full" mbarrier (TMA bytes) and an "empty"
-// mbarrier (one arrival per warp when it has finished reading the stage).
+// Same register outer product as sgemm_ffma.cuh (8 x TN FFMA2 thread tiles in 64 x 4 TN
+// warp tiles, four warps per 128 x 8 TN CTA tile, MINB CTAs per SM), but the operand tiles
+// reach shared memory by TMA instead of per-thread copies: one thread issues two
+// cp.async.bulk.tensor copies per 32-wide K block into a STAGES-deep ring, and the math
+// warps spend no issue slots on address arithmetic or copies (on this GPU those took about
+// 18% of the slots of the copy-based kernel). Each stage has a "full" mbarrier (TMA bytes)
+// and an "empty" mbarrier (one arrival per warp when it has finished reading the stage);
+// the refill of a stage is issued at the start of the next K block, as soon as every warp
+// has released it, so a 2-stage ring still overlaps each copy with a whole K block.
 //
 // Layouts in shared memory:
 //  * A tile: 128 rows (m) x 32 k, as stored (k contiguous), written by TMA with the 128-byte
@@ -15,8 +17,8 @@
 //    are r = lane_m + 8 i, so the eight row groups of a warp hit eight different chunks:
 //    every 128-bit fragment load is conflict-free. One float4 gives a row's values for 4
 //    consecutive k, so A fragments are loaded once per 4 k steps.
-//  * B tile: 32 k x 128 n, as stored (n contiguous), no swizzle; a thread's 16 columns are
-//    four float4 at stride 16 columns, as in the copy-based kernel.
+//  * B tile: 32 k x BN n, as stored (n contiguous), no swizzle; a thread's TN columns are
+//    TN / 4 float4 at stride 16 columns, as in the copy-based kernel.
 // Ragged edges: TMA fills out-of-range rows / columns / k with zeros, so the main loop has
 // no masks; the epilogue masks rows and columns. Every mbarrier wait is bounded; a wait
 // that gives up sets a device status word and the CTA stops computing (the result is then
@@ -31,20 +33,35 @@
 namespace sgemm {
 namespace tma {
 
-constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3, THREADS = 128;
-constexpr int WM = 64, WN = 64, TM = 8, TN = 16, LM = 8, LN = 4, WARPS_N = 2;
-constexpr int A_BYTES = BM * BK * 4, B_BYTES = BK * BN * 4;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 64;  // + alignment slack, barriers
+// BN_ = 8 TN_ columns per CTA; DBA_: double-buffer the A fragments (needs ~32 more
+// registers per thread).
+template <int BN_, int TN_, int STAGES_, int MINB_, bool DBA_>
+struct TmaCfg {
+  static constexpr int BM = 128, BN = BN_, BK = 32, STAGES = STAGES_, THREADS = 128;
+  static constexpr int WM = 64, WN = BN / 2, TM = 8, TN = TN_, LM = 8, LN = 4, WARPS_N = 2;
+  static constexpr int MINB = MINB_;
+  static constexpr bool DBA = DBA_;
+  static constexpr int A_BYTES = BM * BK * 4, B_BYTES = BK * BN * 4;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 64;  // + slack, barriers
 
-static_assert(LM * LN == 32 && WM == LM * TM && WN == LN * TN, "lane layout");
-static_assert((BM / WM) * (BN / WN) * 32 == THREADS, "four warps");
-static_assert(BK * 4 == 128, "A rows are one 128-byte swizzle span");
+  static_assert(LM * LN == 32 && WM == LM * TM && WN == LN * TN, "lane layout");
+  static_assert((BM / WM) * (BN / WN) * 32 == THREADS, "four warps");
+  static_assert(BK * 4 == 128, "A rows are one 128-byte swizzle span");
+  static_assert(STAGE_BYTES % 1024 == 0, "every A stage 1024-byte aligned (swizzle atom)");
+  static_assert(TN % 4 == 0 && BN <= 256, "B box: float4 columns, at most 256 wide");
+  static_assert(STAGES >= 2, "a ring needs two stages");
+};
 
-__global__ void __launch_bounds__(THREADS, 2)
+template <class Cfg>
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
     sgemm_tma_kernel(const __grid_constant__ CUtensorMap map_a,
                      const __grid_constant__ CUtensorMap map_b, const GemmParams p,
                      int *status) {
+  constexpr int BM = Cfg::BM, BN = Cfg::BN, BK = Cfg::BK, STAGES = Cfg::STAGES;
+  constexpr int THREADS = Cfg::THREADS, WM = Cfg::WM, WN = Cfg::WN, TM = Cfg::TM;
+  constexpr int TN = Cfg::TN, LN = Cfg::LN, WARPS_N = Cfg::WARPS_N;
+  constexpr int A_BYTES = Cfg::A_BYTES, STAGE_BYTES = Cfg::STAGE_BYTES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // 128-byte swizzle needs 1024-byte alignment
@@ -120,46 +137,9 @@ __global__ void __launch_bounds__(THREADS, 2)
       if (lane == 0) atomicCAS(status, 0, 1);
       break;
     }
-    const float *as = smem_f + s * (STAGE_BYTES / 4);
-    const float *bs = as + A_BYTES / 4;
-#pragma unroll 1
-    for (int c = 0; c < BK / 4; ++c) {
-      float4 fa[TM];
-#pragma unroll
-      for (int i = 0; i < TM; ++i)
-        fa[i] = *reinterpret_cast<const float4 *>(as + (a_row + 8 * i) * BK + ((c ^ swz) << 2));
-      float4 fb[2][TN / 4];
-#pragma unroll
-      for (int jj = 0; jj < TN / 4; ++jj)
-        fb[0][jj] = *reinterpret_cast<const float4 *>(bs + (4 * c) * BN + b_col0 + 16 * jj);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) {
-        const int cur = kk & 1;
-        if (kk + 1 < 4) {
-#pragma unroll
-          for (int jj = 0; jj < TN / 4; ++jj)
-            fb[cur ^ 1][jj] =
-                *reinterpret_cast<const float4 *>(bs + (4 * c + kk + 1) * BN + b_col0 + 16 * jj);
-        }
-        unsigned long long b2[TN / 2];
-#pragma unroll
-        for (int jj = 0; jj < TN / 4; ++jj) {
-          b2[2 * jj] = pack2(fb[cur][jj].x, fb[cur][jj].y);
-          b2[2 * jj + 1] = pack2(fb[cur][jj].z, fb[cur][jj].w);
-        }
-#pragma unroll
-        for (int i = 0; i < TM; ++i) {
-          const float a = kk == 0 ? fa[i].x : kk == 1 ? fa[i].y : kk == 2 ? fa[i].z : fa[i].w;
-          const unsigned long long a2 = pack2(a, a);
-#pragma unroll
-          for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], a2, b2[j]);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // this warp is done with stage s
     if (tid == 0 && issued < KT) {
-      // refill the stage that k tile kt - 1 used (kt + STAGES - 1 lands there)
+      // refill the stage that k tile kt - 1 used (kt + STAGES - 1 lands there) once every
+      // warp has released it
       if (kt >= 1 && !mbar_wait(bars + 8 * (STAGES + (kt - 1) % STAGES),
                                 (uint32_t)((kt - 1) / STAGES) & 1u)) {
         atomicCAS(status, 0, 2);
@@ -168,6 +148,52 @@ __global__ void __launch_bounds__(THREADS, 2)
         ++issued;
       }
     }
+    const float *as = smem_f + s * (STAGE_BYTES / 4);
+    const float *bs = as + A_BYTES / 4;
+    // Fragments are double-buffered: the A float4s of chunk c + 1 (4 k each) load while
+    // chunk c computes, and the B float4s of step k + 1 while step k computes.
+    constexpr int NA = Cfg::DBA ? 2 : 1;
+    float4 fa[NA][TM], fb[2][TN / 4];
+    auto load_a = [&](int c, int buf) {
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+        fa[buf][i] =
+            *reinterpret_cast<const float4 *>(as + (a_row + 8 * i) * BK + ((c ^ swz) << 2));
+    };
+    auto load_b = [&](int k, int buf) {
+#pragma unroll
+      for (int jj = 0; jj < TN / 4; ++jj)
+        fb[buf][jj] = *reinterpret_cast<const float4 *>(bs + k * BN + b_col0 + 16 * jj);
+    };
+    load_a(0, 0);
+    load_b(0, 0);
+#pragma unroll
+    for (int c = 0; c < BK / 4; ++c) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        const int k = 4 * c + kk;
+        if (Cfg::DBA && kk == 1 && c + 1 < BK / 4) load_a(c + 1, (c + 1) & (NA - 1));
+        if (!Cfg::DBA && kk == 0 && c > 0) load_a(c, 0);
+        if (k + 1 < BK) load_b(k + 1, (k + 1) & 1);
+        const float4 *fac = fa[c & (NA - 1)];
+        const float4 *fbc = fb[k & 1];
+        unsigned long long b2[TN / 2];
+#pragma unroll
+        for (int jj = 0; jj < TN / 4; ++jj) {
+          b2[2 * jj] = pack2(fbc[jj].x, fbc[jj].y);
+          b2[2 * jj + 1] = pack2(fbc[jj].z, fbc[jj].w);
+        }
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+          const float a = kk == 0 ? fac[i].x : kk == 1 ? fac[i].y : kk == 2 ? fac[i].z : fac[i].w;
+          const unsigned long long a2 = pack2(a, a);
+#pragma unroll
+          for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], a2, b2[j]);
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // this warp is done with stage s
   }
   // Thread 0 may not leave while copies it issued are in flight: wait for the last ones.
   if (tid == 0) {

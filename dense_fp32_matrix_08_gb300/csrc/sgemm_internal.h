@@ -20,4 +20,23 @@ cudaMemPool_t workspace_pool();
 bool encode_map_2d(CUtensorMap *map, const float *ptr, long long rows, long long cols,
                    long long ld, int box_cols, int box_rows, bool swizzle128);
 
+struct GemmParams;
+
+// TMA-fed GEMM (sgemm_ffma_tma.cuh): one-time kernel attributes for the current device, and
+// a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb).
+cudaError_t tma_setup();
+cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
+                       const GemmParams &p, int ctas, int *status, cudaStream_t stream);
+
+// K-paired TMA-fed GEMM (sgemm_ffma_kpair.cuh): one-time kernel attributes for the current
+// device, and a launch with the given ring depth (4, 5 or 6 stages).
+cudaError_t kpair_setup();
+cudaError_t launch_kpair(int stages, const CUtensorMap &map_a, const CUtensorMap &map_bt,
+                         const GemmParams &p, int ctas, int *status, cudaStream_t stream);
+
+// Bt = B^T for a K x N row-major B (row stride ldb) into an N x K row-major Bt (row
+// stride ldbt >= K).
+cudaError_t launch_transpose_b(const float *B, long long ldb, int K, int N, float *Bt,
+                               long long ldbt, int num_sms, cudaStream_t stream);
+
 }  // namespace sgemm

@@ -17,6 +17,8 @@ struct Problem {
   int M, N, K, lda, ldb, ldc;
   int transa = 0, transb = 0;  // 1: op(X) = X_st^T (see sgemm_f32_ex)
   bool tma_ok = false;         // A, B 16-byte aligned with lda, ldb % 4 == 0 (TMA-fed kernel)
+  bool kpair_ok = false;       // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
+  bool b_kmajor = false;       // op(B) = B_st^T with B_st 16-byte aligned, ldb % 4 == 0
 };
 
 // Shape of one compiled tile configuration (mirrors TileConfig in sgemm_ffma.cuh).
@@ -26,6 +28,8 @@ struct VariantShape {
   bool automatic;  // considered by the automatic plan (others only when forced)
   bool trans_ok;   // compiled with the transposed-operand copy paths
   bool tma = false;  // the TMA-fed kernel (sgemm_ffma_tma.cuh), aligned row-major operands only
+  bool kpair = false;  // the K-paired TMA-fed kernel (sgemm_ffma_kpair.cuh): K-major B
+  int inst = 0;        // TMA-fed kernels: instance index of the launcher (sgemm_tma.cu)
 };
 
 // mode: 0 scalar FFMA, 1 FFMA2 with register broadcast, 2 FFMA2 with duplicated A in smem
@@ -62,10 +66,22 @@ constexpr VariantShape kVariants[] = {
     {128, 128, 16, 128, 8, 16, 3, 2, 2, smem_of(128, 128, 16, 3, 2), 0.80, false, false},
     // 26: TMA-fed 128 x 128 x 32, 3 stages, 2 CTAs/SM (its own kernel, see kTmaVariant)
     {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 0.96, true, false, true},
+    // 27..29: K-paired TMA-fed 128 x 128 x 32, 8 warps, 1 CTA/SM, 4 / 5 / 6 stages; B is
+    // read K-major (B^T), copied to a workspace first when the caller's B is row-major
+    {128, 128, 32, 256, 8, 8, 4, 1, 3, smem_of(128, 128, 32, 4, 1), 0.88, true, true, false, true},
+    {128, 128, 32, 256, 8, 8, 5, 1, 3, smem_of(128, 128, 32, 5, 1), 0.88, false, true, false, true},
+    {128, 128, 32, 256, 8, 8, 6, 1, 3, smem_of(128, 128, 32, 6, 1), 0.88, false, true, false, true},
+    // 30..32: more TMA-fed shapes: 128 x 96 (8 x 12 threads, 3 CTAs/SM, 2 stages); the 26
+    // shape without A double-buffering; 128 x 64 (8 x 8 threads, 4 CTAs/SM, 2 stages)
+    {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1), 0.97, true, false, true, false, 1},
+    {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 0.90, false, false, true, false, 2},
+    {128, 64, 32, 128, 8, 8, 2, 4, 1, smem_of(128, 64, 32, 2, 1), 0.955, true, false, true, false, 3},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;
+constexpr int kFirstKpairVariant = 27;
 static_assert(kVariants[kTmaVariant].tma, "TMA variant index");
+static_assert(kVariants[kFirstKpairVariant].kpair, "K-paired variant index");
 
 struct Plan {
   int variant = -1;     // -1: no GEMM kernel (beta-scale only, or nothing)
@@ -76,7 +92,9 @@ struct Plan {
   int group_m = 1;
   int ctas = 0;         // GEMM grid size
   int launches = 0;
-  size_t ws_bytes = 0;
+  size_t ws_bytes = 0;  // B^T copy (bt_bytes, first) + split-K partial tiles
+  size_t bt_bytes = 0;  // K-paired variants on a row-major B: its N x ldbt transpose
+  long long ldbt = 0;
   double cycles = 0;    // modelled cost
 };
 
@@ -193,14 +211,20 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   } else {
     gemm_bytes += mn_c;
   }
+  double bt_cycles = 0.0;
+  if (s.kpair && !p.b_kmajor) {  // B -> B^T copy: K N floats read and written, one launch
+    pl.ldbt = ceil_div(p.K, 4) * 4;
+    pl.bt_bytes = (size_t)ceil_div((long long)p.N * pl.ldbt * 4, 256) * 256;
+    bt_cycles = 8.0 * (double)p.K * p.N / 3400.0 + 2000.0;
+  }
   pl.main_tiles = (int)main;
   pl.split = split;
   pl.k_per_split = (int)(kt_per * s.BK);
   pl.group_m = std::min(16, pl.tiles_m);
   pl.ctas = (int)(main + slices);
-  pl.launches = slices > 0 ? 2 : 1;
-  pl.ws_bytes = slices > 0 ? (size_t)part_bytes : 0;
-  pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce;
+  pl.launches = (slices > 0 ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0);
+  pl.ws_bytes = pl.bt_bytes + (slices > 0 ? (size_t)part_bytes : 0);
+  pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce + bt_cycles;
   if (main + slices > 0x7fffffffLL) {  // grid too large for one launch
     pl.ctas = 0;
     pl.cycles = std::numeric_limits<double>::infinity();
@@ -214,7 +238,10 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
 // force_v >= 0 pins the variant. force_split >= 1 splits every tile into that many slices
 // (1: none); force_split == -1 takes the whole-waves-plus-split-tail layout with the
 // automatic slice count, force_split <= -2 the same layout with -force_split slices;
-// 0 leaves the choice to the model.
+// 0 leaves the choice to the model. The automatic choice takes the K-paired configurations
+// only for a B that is already K-major (transposed and aligned): copying a row-major B to
+// B^T first is never faster than the TMA-fed configuration on the same operands, so that
+// copy happens only when such a configuration is forced.
 inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, int force_v,
                       int force_split) {
   Plan best;
@@ -227,8 +254,10 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   const bool beta_nz = beta != 0.0f;
   best.cycles = std::numeric_limits<double>::infinity();
   const double ws_cap = 64.0 * 1024 * 1024;  // largest split-K workspace the plan may use
+  const size_t bt_cap = (size_t)2 << 30;       // largest B^T copy the plan may make
   auto consider = [&](const Plan &c) {
-    if ((double)c.ws_bytes > ws_cap && force_split < 1) return;
+    if ((double)(c.ws_bytes - c.bt_bytes) > ws_cap && force_split < 1) return;
+    if (c.bt_bytes > bt_cap) return;
     if (c.cycles < best.cycles * 0.999) best = c;  // prefer earlier (simpler) on ties
   };
   const int v_lo = force_v >= 0 ? force_v : 0;
@@ -238,6 +267,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
     if (force_v < 0 && !kVariants[v].automatic) continue;
     if (trans && !kVariants[v].trans_ok) continue;
     if (kVariants[v].tma && !p.tma_ok) continue;
+    if (kVariants[v].kpair && (!p.kpair_ok || (force_v < 0 && !p.b_kmajor))) continue;
     const VariantShape &s = kVariants[v];
     const long long tiles = ceil_div(p.M, s.BM) * ceil_div(p.N, s.BN);
     const long long kt = ceil_div(p.K, s.BK);
@@ -258,9 +288,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
     }
     consider(model_plan(p, v, tiles, 1, num_sms, beta_nz));
     for (int sp = 2; sp <= max_split; ++sp) consider(model_plan(p, v, 0, sp, num_sms, beta_nz));
-    // Split tails only for one-CTA-per-SM configurations: with several CTAs per SM a
-    // partial last wave already runs with fewer CTAs per SM, each of them faster.
-    if (main > 0 && tail > 0 && s.min_blocks == 1) {
+    if (main > 0 && tail > 0) {
       const int sp = (int)std::min<long long>(max_split, std::max<long long>(2, slots / tail));
       consider(model_plan(p, v, main, sp, num_sms, beta_nz));
     }

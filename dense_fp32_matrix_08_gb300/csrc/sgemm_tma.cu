@@ -1,0 +1,69 @@
+// Instantiations and launcher of the TMA-fed FFMA2 GEMM (sgemm_ffma_tma.cuh).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "sgemm_ffma_tma.cuh"
+#include "sgemm_internal.h"
+
+namespace sgemm {
+namespace {
+
+// Instance table: index = VariantShape::inst of the TMA-fed variants in sgemm_plan.h.
+using Tma0 = tma::TmaCfg<128, 16, 3, 2, true>;   // 128 x 128, 8 x 16 threads, 2 CTAs/SM
+using Tma1 = tma::TmaCfg<96, 12, 2, 3, false>;   // 128 x 96, 8 x 12 threads, 3 CTAs/SM
+using Tma2 = tma::TmaCfg<128, 16, 3, 2, false>;  // Tma0 without A double-buffering
+using Tma3 = tma::TmaCfg<64, 8, 2, 4, false>;    // 128 x 64, 8 x 8 threads, 4 CTAs/SM
+constexpr int kInstances = 4;
+
+std::once_flag g_once[64];
+cudaError_t g_err[64];
+
+template <class Cfg>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(tma::sgemm_tma_kernel<Cfg>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM_BYTES);
+}
+
+template <class Cfg>
+cudaError_t launch(const float *A, long long lda, const float *B, long long ldb,
+                   const GemmParams &p, int ctas, int *status, cudaStream_t stream) {
+  CUtensorMap map_a, map_b;
+  if (!encode_map_2d(&map_a, A, p.M, p.K, lda, Cfg::BK, Cfg::BM, true) ||
+      !encode_map_2d(&map_b, B, p.K, p.N, ldb, Cfg::BN, Cfg::BK, false))
+    return cudaErrorInvalidValue;
+  tma::sgemm_tma_kernel<Cfg><<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(map_a, map_b, p,
+                                                                             status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t tma_setup() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::call_once(g_once[dev], [dev]() {
+    cudaError_t err = set_smem<Tma0>();
+    if (err == cudaSuccess) err = set_smem<Tma1>();
+    if (err == cudaSuccess) err = set_smem<Tma2>();
+    if (err == cudaSuccess) err = set_smem<Tma3>();
+    g_err[dev] = err;
+  });
+  return g_err[dev];
+}
+
+cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
+                       const GemmParams &p, int ctas, int *status, cudaStream_t stream) {
+  static_assert(kInstances == 4, "instance table");
+  switch (inst) {
+    case 0: return launch<Tma0>(A, lda, B, ldb, p, ctas, status, stream);
+    case 1: return launch<Tma1>(A, lda, B, ldb, p, ctas, status, stream);
+    case 2: return launch<Tma2>(A, lda, B, ldb, p, ctas, status, stream);
+    case 3: return launch<Tma3>(A, lda, B, ldb, p, ctas, status, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace sgemm

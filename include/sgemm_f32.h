@@ -168,11 +168,20 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
  * (1: no split-K); -1 computes the full waves of tiles whole and splits only the tiles of
  * the last, partial wave (slice count chosen to fill it); <= -2 does the same with
  * -split slices; 0 is automatic. Slice counts are clamped so that every slice holds at
- * least one K tile. Returns -14 for an out-of-range variant, or for the TMA-fed
- * configuration when A or B is not 16-byte aligned with lda, ldb multiples of 4. */
+ * least one K tile. Returns -14 for an out-of-range variant, for the TMA-fed
+ * configuration when A or B is not 16-byte aligned with lda, ldb multiples of 4, and for
+ * the K-paired configurations when A is not. */
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);
+
+/* sgemm_f32_ex with the plan forced (variant and split as in sgemm_f32_forced). Returns
+ * -14 also when the forced configuration has no path for these transpose flags or this
+ * alignment: the TMA-fed configuration needs transa = transb = 0; the K-paired ones need
+ * transa = 0 and A 16-byte aligned with lda a multiple of 4. */
+int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha,
+                        const float *A, int lda, const float *B, int ldb, float beta, float *C,
+                        int ldc, int variant, int split, cudaStream_t stream);
 
 /* Size of the fixed device scratch array used by sgemm_f32_noalloc, and its error code. */
 #define SGEMM_F32_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20) /* 32 MiB per device */

@@ -15,8 +15,9 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 27  # compiled tile configurations; checked against the library below
-TMA_VARIANT = 26   # the TMA-fed kernel (aligned, row-major operands only)
+NUM_VARIANTS = 33  # compiled tile configurations; checked against the library below
+TMA_VARIANTS = (26, 30, 31, 32)  # every TMA-fed instance
+KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -106,12 +107,15 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
-    if not aligned and variant == TMA_VARIANT:
+    if not aligned and variant in TMA_VARIANTS:
         pytest.skip("the TMA-fed configuration needs aligned operands")
     for (M, N, K) in RAGGED:
         A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
-        if aligned and variant == TMA_VARIANT:  # TMA needs ld % 4 == 0: pad the rows
+        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS:
+            # TMA needs ld % 4 == 0: pad the rows
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
+        elif variant in KPAIR_VARIANTS:  # aligned A; B and C with odd ld and offsets
+            lds, offs = (-(-K // 4) * 4, N + 3, N + 5), (0, 3, 5)
         elif aligned:
             lds, offs = (None, None, None), (0, 0, 0)
         else:  # odd leading dimensions and odd element offsets: 32-bit paths everywhere
@@ -161,12 +165,14 @@ def test_tma_variant_refuses_unaligned():
     dA, _ = to_device_view(A, 65, 1)
     dB, _ = to_device_view(B)
     dC, _ = to_device_view(C)
-    assert sg.sgemm_f32_forced(64, 64, 64, 1.0, dA, 65, dB, 64, 0.0, dC, 64, TMA_VARIANT, 1) == -14
+    for v in TMA_VARIANTS + KPAIR_VARIANTS:
+        assert sg.sgemm_f32_forced(64, 64, 64, 1.0, dA, 65, dB, 64, 0.0, dC, 64, v, 1) == -14
 
 
 def test_status_words_clear():
     A, B, C = make_inputs(300, 300, 300, seed=13)
-    out, _ = _run(A, B, C, 1.0, 0.5, variant=TMA_VARIANT, split=1)
+    for v in TMA_VARIANTS + KPAIR_VARIANTS:
+        out, _ = _run(A, B, C, 1.0, 0.5, variant=v, split=1)
     assert sg.sgemm_f32_status() == (0, 0)
 
 
