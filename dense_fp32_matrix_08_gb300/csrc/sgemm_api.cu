@@ -13,6 +13,7 @@
 #include "../../include/sgemm_f32.h"
 #include "sgemm_aux.cuh"
 #include "sgemm_ffma_kpair.cuh"
+#include "sgemm_thin.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_plan.h"
 #include "sgemm_variants.cuh"
@@ -30,9 +31,12 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},  // more TMA-fed instances (sgemm_tma.cu)
     VariantKernels{},
     VariantKernels{},
+    VariantKernels{},  // thin-M and thin-N streaming kernels (sgemm_thin.cu)
+    VariantKernels{},
 };
-static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kNumVariants == 33,
-              "the generic variants come first, then the TMA-fed ones");
+static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
+                  kThinNVariant == 34 && kNumVariants == 35,
+              "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
 __device__ int g_ffma_status;
@@ -67,6 +71,7 @@ cudaError_t device_setup(int *num_sms) {
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kKernels[v].smem);
     if (err == cudaSuccess) err = tma_setup();
+    if (err == cudaSuccess) err = thin_setup();
     if (err == cudaSuccess) err = kpair_setup();
     if (err == cudaSuccess)
       err = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_ffma_status);
@@ -159,6 +164,40 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     return (int)cudaGetLastError();
   }
   const VariantShape &vs = kVariants[pl.variant];
+  if (vs.thin) {
+    thin::ThinParams tp;
+    tp.M = pr.M;
+    tp.N = pr.N;
+    tp.K = pr.K;
+    tp.alpha = alpha;
+    tp.beta = beta;
+    tp.A = A;
+    tp.lda = pr.lda;
+    tp.B = B;
+    tp.ldb = pr.ldb;
+    tp.C = C;
+    tp.ldc = pr.ldc;
+    tp.ws = ws;
+    tp.split = pl.split;
+    tp.k_per_split = pl.k_per_split;
+    tp.tiles_m = pl.tiles_m;
+    tp.tiles_n = pl.tiles_n;
+    tp.vec_c = vec_c ? 1 : 0;
+    // 128-bit loads of the streamed operand: B rows (thin-M) or A rows (thin-N)
+    const bool vec = vs.thin == 1 ? (pr.ldb % 4 == 0 && aligned16(B))
+                                  : (pr.lda % 4 == 0 && aligned16(A));
+    cudaError_t te = launch_thin(vs.thin == 1, tp, vec, stream);
+    if (te != cudaSuccess) return (int)te;
+    if (pl.split > 1) {
+      const long long tiles = (long long)pl.tiles_m * pl.tiles_n;
+      const long long work = tiles * vs.BM * (vs.BN / 4);
+      tail_reduce_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+          ws, 0, (int)tiles, pl.split, vs.BM, vs.BN, pl.tiles_m, pl.tiles_n, 1, pr.M, pr.N,
+          alpha, beta, C, pr.ldc, vec_c ? 1 : 0);
+      te = cudaGetLastError();
+    }
+    return (int)te;
+  }
   GemmParams p;
   p.M = pr.M;
   p.N = pr.N;

@@ -21,6 +21,15 @@ bool encode_map_2d(CUtensorMap *map, const float *ptr, long long rows, long long
                    long long ld, int box_cols, int box_rows, bool swizzle128);
 
 struct GemmParams;
+namespace thin {
+struct ThinParams;
+}
+
+// Thin-product streaming kernels (sgemm_thin.cuh): one-time kernel attributes for the
+// current device, and a launch (thin_m: the thin-M kernel, else thin-N; vec: 128-bit loads
+// of the streamed operand allowed).
+cudaError_t thin_setup();
+cudaError_t launch_thin(bool thin_m, const thin::ThinParams &p, bool vec, cudaStream_t stream);
 
 // TMA-fed GEMM (sgemm_ffma_tma.cuh): one-time kernel attributes for the current device, and
 // a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb).

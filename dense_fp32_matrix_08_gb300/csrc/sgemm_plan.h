@@ -30,6 +30,7 @@ struct VariantShape {
   bool tma = false;  // the TMA-fed kernel (sgemm_ffma_tma.cuh), aligned row-major operands only
   bool kpair = false;  // the K-paired TMA-fed kernel (sgemm_ffma_kpair.cuh): K-major B
   int inst = 0;        // TMA-fed kernels: instance index of the launcher (sgemm_tma.cu)
+  int thin = 0;        // streaming kernels of sgemm_thin.cuh: 1 thin-M, 2 thin-N
 };
 
 // mode: 0 scalar FFMA, 1 FFMA2 with register broadcast, 2 FFMA2 with duplicated A in smem
@@ -76,10 +77,18 @@ constexpr VariantShape kVariants[] = {
     {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1), 0.97, true, false, true, false, 1},
     {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 0.90, false, false, true, false, 2},
     {128, 64, 32, 128, 8, 8, 2, 4, 1, smem_of(128, 64, 32, 2, 1), 0.955, true, false, true, false, 3},
+    // 33, 34: streaming kernels for thin products (sgemm_thin.cuh): thin-M, 16 x 256 C tiles
+    // (4 columns x 16 rows per thread, 4 k-groups, 2 CTAs/SM); thin-N, 1024 x 16 C tiles
+    // (4 rows x 16 columns per thread, 1 CTA/SM). BK is the k batch of the streamed loads.
+    {16, 256, 8, 256, 16, 4, 1, 2, 1, 0, 0.65, false, false, false, false, 0, 1},
+    {1024, 16, 8, 256, 4, 16, 1, 1, 1, 0, 0.65, false, false, false, false, 0, 2},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;
 constexpr int kFirstKpairVariant = 27;
+constexpr int kThinMVariant = 33, kThinNVariant = 34;
+constexpr int kThinMaxDim = 64;  // thin kernels considered for M (thin-M) or N (thin-N) <= this
+constexpr int kThinMKmax = 512, kThinNKmax = 2048;  // K slice bounds (shared memory)
 static_assert(kVariants[kTmaVariant].tma, "TMA variant index");
 static_assert(kVariants[kFirstKpairVariant].kpair, "K-paired variant index");
 
@@ -99,6 +108,47 @@ struct Plan {
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Modelled cost of a thin-product streaming kernel (variant v with s.thin != 0) with `split`
+// K slices. Both kernels stream one operand once and are bound by HBM at their shapes:
+// the cost is the larger of the streamed bytes at ~2800 bytes/cycle for the chip (about
+// 80% of the measured copy bandwidth) and the FMA work at the variant's efficiency, plus
+// ~2000 cycles per launch. Partial tiles add their write and the reduce's read.
+inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool beta_nz) {
+  const VariantShape &s = kVariants[v];
+  Plan pl;
+  pl.variant = v;
+  pl.tiles_m = (int)ceil_div(p.M, s.BM);
+  pl.tiles_n = (int)ceil_div(p.N, s.BN);
+  const int kmax = s.thin == 1 ? kThinMKmax : kThinNKmax;
+  long long kps = ceil_div(ceil_div(p.K, std::max(1, split)), 8) * 8;
+  kps = std::min<long long>(std::max<long long>(kps, 8), kmax);
+  split = (int)ceil_div(p.K, kps);
+  const long long tiles = (long long)pl.tiles_m * pl.tiles_n;
+  const long long ctas = tiles * split;
+  const double per_cta_fma = (double)s.BM * s.BN * (double)kps;
+  const double rate = 128.0 * s.eff / s.min_blocks;  // FMA per cycle per resident CTA
+  const long long slots = (long long)num_sms * s.min_blocks;
+  const double compute = (double)ceil_div(ctas, slots) * per_cta_fma / rate;
+  // streamed operand once per tile row (thin-M: B per row block) or column (thin-N: A)
+  const double streamed = s.thin == 1 ? 4.0 * pl.tiles_m * (double)p.K * p.N
+                                      : 4.0 * pl.tiles_n * (double)p.M * p.K;
+  const double small = s.thin == 1 ? 4.0 * (double)p.M * p.K : 4.0 * (double)p.K * p.N;
+  const double part = split > 1 ? (double)ctas * s.BM * s.BN * 4.0 : 0.0;
+  const double mn_c = (double)p.M * p.N * 4.0 * (beta_nz ? 2.0 : 1.0);
+  const double bytes = streamed + small + mn_c + 2.0 * part;
+  pl.main_tiles = 0;
+  pl.split = split;
+  pl.k_per_split = (int)kps;
+  pl.group_m = 1;
+  pl.ctas = (int)std::min<long long>(ctas, 0x7fffffffLL);
+  pl.launches = split > 1 ? 2 : 1;
+  pl.ws_bytes = split > 1 ? (size_t)part : 0;
+  pl.cycles = std::max(compute, bytes / 2800.0) + 2000.0 * pl.launches;
+  if (ctas > 0x7fffffffLL || pl.tiles_m > 65535 || pl.tiles_n > 65535 || split > 65535)
+    pl.cycles = std::numeric_limits<double>::infinity();
+  return pl;
+}
 
 // BLAS-style check: the first illegal argument, numbered from 1 in the sgemm_f32 order
 // (M, N, K, alpha, A, lda, B, ldb, beta, C, ldc). A and B only have to be present when
@@ -269,6 +319,18 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
     if (kVariants[v].tma && !p.tma_ok) continue;
     if (kVariants[v].kpair && (!p.kpair_ok || (force_v < 0 && !p.b_kmajor))) continue;
     const VariantShape &s = kVariants[v];
+    if (s.thin) {
+      if (force_v < 0 && (s.thin == 1 ? p.M : p.N) > kThinMaxDim) continue;
+      const int kmax = s.thin == 1 ? kThinMKmax : kThinNKmax;
+      const int min_split = (int)ceil_div(p.K, kmax);
+      if (force_split >= 1) {
+        consider(model_thin(p, v, std::max(force_split, min_split), num_sms, beta_nz));
+        continue;
+      }
+      for (int sp = min_split; sp <= std::max(min_split, 96); ++sp)
+        consider(model_thin(p, v, sp, num_sms, beta_nz));
+      continue;
+    }
     const long long tiles = ceil_div(p.M, s.BM) * ceil_div(p.N, s.BN);
     const long long kt = ceil_div(p.K, s.BK);
     const int max_split = (int)std::min<long long>(64, kt);

@@ -15,9 +15,10 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 33  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 35  # compiled tile configurations; checked against the library below
 TMA_VARIANTS = (26, 30, 31, 32)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
+THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -151,6 +152,32 @@ def test_ragged_sweep_auto_plan():
         assert guard, (M, N, K)
         R, S = oracle.sgemm_f64(A, B, C, 1.0, 0.5)
         assert_bound(out.numpy(), R, S, 0.5, C.numpy(), f"auto {M,N,K}")
+
+
+THIN_M_SHAPES = [(1, 1, 1), (5, 255, 7), (16, 256, 513), (16, 1000, 2049), (13, 4100, 64),
+                 (16, 4096, 1100)]
+THIN_N_SHAPES = [(1, 1, 1), (255, 5, 7), (1024, 16, 2049), (1000, 16, 4100), (4100, 13, 64),
+                 (3000, 16, 1100)]
+
+
+@pytest.mark.parametrize("kind", ["m", "n"])
+@pytest.mark.parametrize("split", [0, 1, 5])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_thin_kernels(kind, split, aligned):
+    """The thin-M / thin-N streaming kernels, forced, on ragged and slice-boundary shapes:
+    K slices that are not a multiple of the 8-deep load batch, column quads and rows that
+    cross N and M, one slice (alpha / beta in the kernel) and several (reduce kernel)."""
+    variant = THIN_M if kind == "m" else THIN_N
+    for (M, N, K) in (THIN_M_SHAPES if kind == "m" else THIN_N_SHAPES):
+        A, B, C = make_inputs(M, N, K, seed=M + 3 * N + 5 * K + split)
+        if aligned:
+            lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
+        else:
+            lds, offs = (K + 1, N + 3, N + 5), (1, 3, 5)
+        out, guard = _run(A, B, C, 0.75, -1.25, *lds, offs=offs, variant=variant, split=split)
+        assert guard, (M, N, K)
+        R, S = oracle.sgemm_f64(A, B, C, 0.75, -1.25)
+        assert_bound(out.numpy(), R, S, -1.25, C.numpy(), f"thin-{kind} s{split} {M,N,K}")
 
 
 # --------------------------------------------------------------------------------------
