@@ -21,7 +21,8 @@ __all__ = [
     "sgemm_f32_variant_info", "sgemm_f32_version", "sgemm_f32_noalloc", "sgemm_f32_ex",
     "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_status", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
-    "sgemm", "EXPORTED",
+    "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
+    "sgemm_f32_tune_load", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -31,7 +32,8 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemv_f32", "sdot_f32", "sgemm_f32_status",
             "sgemm_f32_3xtf32",
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status",
-            "sgemm_f32_ex_forced")
+            "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
+            "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load")
 
 
 class SgemmError(RuntimeError):
@@ -58,6 +60,11 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_noalloc.argtypes = gemm + [vp]
     L.sgemm_f32_ex.argtypes = [i, i] + gemm + [vp]
     L.sgemm_f32_ex_forced.argtypes = [i, i] + gemm + [i, i, vp]
+    L.sgemm_f32_autotune.argtypes = [i, i] + gemm + [i, vp, pi, pi, ctypes.POINTER(f)]
+    L.sgemm_f32_tune_count.argtypes = []
+    L.sgemm_f32_tune_clear.argtypes = []
+    L.sgemm_f32_tune_save.argtypes = [ctypes.c_char_p]
+    L.sgemm_f32_tune_load.argtypes = [ctypes.c_char_p]
     L.sgemv_f32.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     L.sdot_f32.argtypes = [i, vp, i, vp, i, vp, vp]
     L.sgemm_f32_colmajor.argtypes = [i, i] + gemm + [vp]
@@ -128,6 +135,34 @@ def sgemm_f32_ex_forced(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C,
     return lib.sgemm_f32_ex_forced(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda,
                                    _ptr(B), ldb, beta, _ptr(C), ldc, variant, split,
                                    _stream(stream))
+
+
+def sgemm_f32_autotune(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, reps=3,
+                       stream=None) -> dict:
+    """Time every configuration that can run this problem and record the fastest for its
+    shape (see include/sgemm_f32.h). C is only read. Returns {"status", "variant", "split",
+    "ms"}."""
+    v, sp, ms = ctypes.c_int(-1), ctypes.c_int(0), ctypes.c_float(0.0)
+    rc = lib.sgemm_f32_autotune(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda,
+                                _ptr(B), ldb, beta, _ptr(C), ldc, int(reps), _stream(stream),
+                                ctypes.byref(v), ctypes.byref(sp), ctypes.byref(ms))
+    return {"status": rc, "variant": v.value, "split": sp.value, "ms": ms.value}
+
+
+def sgemm_f32_tune_count() -> int:
+    return lib.sgemm_f32_tune_count()
+
+
+def sgemm_f32_tune_clear() -> int:
+    return lib.sgemm_f32_tune_clear()
+
+
+def sgemm_f32_tune_save(path) -> int:
+    return lib.sgemm_f32_tune_save(os.fsencode(path))
+
+
+def sgemm_f32_tune_load(path) -> int:
+    return lib.sgemm_f32_tune_load(os.fsencode(path))
 
 
 def sgemm_f32_noalloc(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:

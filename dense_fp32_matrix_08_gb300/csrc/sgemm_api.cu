@@ -285,6 +285,13 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
+  if (force_v < 0 && force_split == 0) {  // a plan measured by sgemm_f32_autotune wins
+    int tv = -1, ts = 0;
+    if (tuned_lookup(pr, beta != 0.0f, num_sms, &tv, &ts)) {
+      force_v = tv;
+      force_split = ts;
+    }
+  }
   Plan pl = cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
   // No candidate fitted (a forced configuration whose workspace exceeds the limits).
   if (pl.variant < 0 && alpha != 0.0f && K > 0) return force_v >= 0 ? kErrBadVariant
@@ -394,7 +401,11 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
   if (M == 0 || N == 0) {
     pl.variant = -1;
   } else {
-    pl = cached_plan(pr, alpha, beta, num_sms, -1, 0);
+    int tv = -1, ts = 0;
+    if (tuned_lookup(pr, beta != 0.0f, num_sms, &tv, &ts))
+      pl = cached_plan(pr, alpha, beta, num_sms, tv, ts);
+    else
+      pl = cached_plan(pr, alpha, beta, num_sms, -1, 0);
   }
   if (variant) *variant = pl.variant;
   if (split) *split = pl.split;

@@ -21,6 +21,11 @@ bool encode_map_2d(CUtensorMap *map, const float *ptr, long long rows, long long
                    long long ld, int box_cols, int box_rows, bool swizzle128);
 
 struct GemmParams;
+struct Problem;
+
+// Plan recorded by sgemm_f32_autotune for this problem (shape, flags, beta != 0) on a GPU
+// with num_sms SMs: the forced variant and split to use. False when none is recorded.
+bool tuned_lookup(const Problem &pr, bool beta_nz, int num_sms, int *variant, int *split);
 namespace thin {
 struct ThinParams;
 }

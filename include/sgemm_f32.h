@@ -250,6 +250,47 @@ int sgemm_f32_3xtf32_status(int *status);
  * stopped computing and the result of that call is not valid. */
 int sgemm_f32_status(int *status);
 
+/* ---- Measured plan selection ("GPU GEMM 优化完全拆解（二）", autotuning section: sweep the
+ * legal tile parameters and keep the fastest set, which differs from GPU to GPU). ----
+ *
+ * sgemm_f32_autotune times, on `stream` and the caller's operands, every compiled tile
+ * configuration that can run op(A) op(B) for these transpose flags, shape, leading
+ * dimensions and alignments. Each is timed with three split-K layouts: the model's own
+ * choice, no split, and whole waves plus a split last wave. Each candidate runs once to
+ * warm up, then `reps` times (3 if reps <= 0), timed with CUDA events. Layouts the cost
+ * model rates at more than 4x its best are skipped. The fastest candidate is recorded in
+ * a per-process table. From then on sgemm_f32, sgemm_f32_ex, sgemm_f32_ws,
+ * sgemm_f32_noalloc and sgemm_f32_plan use it instead of the model for the same shape,
+ * transpose flags, alignment class (TMA-able or not), beta != 0 and SM count.
+ * Arguments are those of sgemm_f32_ex. C is only read: the timed calls write a scratch
+ * copy taken from the library's workspace pool. The call synchronises `stream`.
+ * Outputs (any may be NULL): the chosen variant (as in sgemm_f32_forced), the split
+ * argument that reproduces its layout, and its mean time in ms. An empty problem,
+ * alpha == 0 or K == 0 records nothing and returns 0 with *variant = -1.
+ * Returns 0, the sgemm_f32_ex codes for illegal arguments, or a cudaError_t. A recorded
+ * plan may need more workspace than the model's choice. sgemm_f32_ws and
+ * sgemm_f32_noalloc then return -13 / -15 for that shape, as they do for any plan that
+ * does not fit. */
+int sgemm_f32_autotune(int transa, int transb, int M, int N, int K, float alpha,
+                       const float *A, int lda, const float *B, int ldb, float beta,
+                       const float *C, int ldc, int reps, cudaStream_t stream, int *variant,
+                       int *split, float *ms);
+
+/* Number of recorded plans; forget them all (returns 0). */
+int sgemm_f32_tune_count(void);
+int sgemm_f32_tune_clear(void);
+
+/* Write the recorded plans to a text file: two comment lines, then one line per plan,
+ * "sms M N K flags variant split ms". Returns the number of plans written, -1 for a NULL
+ * path, -2 if the file cannot be written. */
+int sgemm_f32_tune_save(const char *path);
+
+/* Add the plans of a file written by sgemm_f32_tune_save (a plan for the same key
+ * replaces the recorded one). Lines whose fields are out of range are skipped. Returns
+ * the number of plans loaded, -1 for a NULL path, -2 if the file cannot be read, or -3 if
+ * any line was skipped (the valid ones are still loaded). */
+int sgemm_f32_tune_load(const char *path);
+
 /* Library version string, e.g. "sgemm_f32 0.1.0 sm_103a". */
 const char *sgemm_f32_version(void);
 
