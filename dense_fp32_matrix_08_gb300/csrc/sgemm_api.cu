@@ -115,7 +115,8 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   const unsigned flags = (alpha == 0.0f ? 1u : 0u) | (beta != 0.0f ? 2u : 0u) |
                          (beta == 1.0f ? 4u : 0u) | (pr.transa ? 8u : 0u) |
                          (pr.transb ? 16u : 0u) | (pr.tma_ok ? 32u : 0u) |
-                         (pr.kpair_ok ? 64u : 0u) | (pr.b_kmajor ? 128u : 0u);
+                         (pr.kpair_ok ? 64u : 0u) | (pr.b_kmajor ? 128u : 0u) |
+                         (pr.a_tma ? 256u : 0u) | (pr.b_tma ? 512u : 0u);
   for (int i = 0; i < kEntries; ++i) {
     const Entry &e = cache[i];
     if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
@@ -239,7 +240,33 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     if (ke != cudaSuccess) return (int)ke;
   } else if (vs.tma) {
     if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
-    cudaError_t ke = launch_tma(vs.inst, A, pr.lda, B, pr.ldb, p, pl.ctas, status_word(), stream);
+    // operands TMA cannot address are copied to aligned rows in the workspace first
+    char *wsb = reinterpret_cast<char *>(ws);
+    const float *Ap = A, *Bp = B;
+    long long ldap = pr.lda, ldbp = pr.ldb;
+    if (pl.pack_a) {
+      float *dst = reinterpret_cast<float *>(wsb + pl.bt_bytes);
+      const long long work = (long long)pr.M * ((pr.K + 3) / 4);
+      pack_rows_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+          A, pr.lda, pr.M, pr.K, dst, pl.lda_p);
+      Ap = dst;
+      ldap = pl.lda_p;
+    }
+    if (pl.pack_b) {
+      float *dst = reinterpret_cast<float *>(wsb + pl.bt_bytes + pl.pack_a_bytes);
+      const long long work = (long long)pr.K * ((pr.N + 3) / 4);
+      pack_rows_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+          B, pr.ldb, pr.K, pr.N, dst, pl.ldb_p);
+      Bp = dst;
+      ldbp = pl.ldb_p;
+    }
+    if (pl.pre_bytes > 0) {
+      p.ws = reinterpret_cast<float *>(wsb + pl.pre_bytes);
+      ws = p.ws;
+    }
+    cudaError_t ke = cudaGetLastError();
+    if (ke == cudaSuccess)
+      ke = launch_tma(vs.inst, Ap, ldap, Bp, ldbp, p, pl.ctas, status_word(), stream);
     if (ke != cudaSuccess) return (int)ke;
   } else {
   const int apath = !pr.transa ? APATH_N
@@ -275,12 +302,14 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
               aligned16(B) && A != nullptr && B != nullptr;
   pr.kpair_ok = !transa && lda % 4 == 0 && aligned16(A) && A != nullptr && B != nullptr;
   pr.b_kmajor = transb && ldb % 4 == 0 && aligned16(B);
+  pr.a_tma = !transa && lda % 4 == 0 && aligned16(A) && A != nullptr;
+  pr.b_tma = !transb && ldb % 4 == 0 && aligned16(B) && B != nullptr;
   int rc = (transa || transb) ? validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr)
                               : validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
   if (rc != 0) return rc;
   if (M == 0 || N == 0) return 0;
   if (force_v >= kNumVariants || force_v < -1) return kErrBadVariant;
-  if (force_v >= 0 && kVariants[force_v].tma && !pr.tma_ok) return kErrBadVariant;
+  if (force_v >= 0 && kVariants[force_v].tma && (transa || transb)) return kErrBadVariant;
   if (force_v >= 0 && kVariants[force_v].kpair && !pr.kpair_ok) return kErrBadVariant;
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
@@ -391,6 +420,8 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
   Problem pr{M, N, K, lda, ldb, ldc};
   pr.tma_ok = lda % 4 == 0 && ldb % 4 == 0;  // pointers assumed 16-byte aligned
   pr.kpair_ok = lda % 4 == 0;
+  pr.a_tma = lda % 4 == 0;
+  pr.b_tma = ldb % 4 == 0;
   int rc = validate(pr, alpha, true, true, true);
   if (rc != 0) return rc;
   if (num_sms <= 0) {

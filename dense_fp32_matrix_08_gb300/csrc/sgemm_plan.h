@@ -17,6 +17,8 @@ struct Problem {
   int M, N, K, lda, ldb, ldc;
   int transa = 0, transb = 0;  // 1: op(X) = X_st^T (see sgemm_f32_ex)
   bool tma_ok = false;         // A, B 16-byte aligned with lda, ldb % 4 == 0 (TMA-fed kernel)
+  bool a_tma = false;          // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
+  bool b_tma = false;          // op(B) = B row-major, 16-byte aligned, ldb % 4 == 0
   bool kpair_ok = false;       // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
   bool b_kmajor = false;       // op(B) = B_st^T with B_st 16-byte aligned, ldb % 4 == 0
 };
@@ -101,9 +103,17 @@ struct Plan {
   int group_m = 1;
   int ctas = 0;         // GEMM grid size
   int launches = 0;
-  size_t ws_bytes = 0;  // B^T copy (bt_bytes, first) + split-K partial tiles
+  // Workspace layout: [B^T copy | packed A | packed B | split-K partial tiles]; the first
+  // three (pre_bytes in all) are written by pre-passes before the GEMM kernel.
+  size_t ws_bytes = 0;
   size_t bt_bytes = 0;  // K-paired variants on a row-major B: its N x ldbt transpose
   long long ldbt = 0;
+  // TMA-fed variants on row-major operands that TMA cannot address (ld % 4 != 0 or a
+  // misaligned pointer): the operand is first copied to rows of ld_p = ceil4(cols) floats.
+  bool pack_a = false, pack_b = false;
+  long long lda_p = 0, ldb_p = 0;
+  size_t pack_a_bytes = 0, pack_b_bytes = 0;
+  size_t pre_bytes = 0;
   double cycles = 0;    // modelled cost
 };
 
@@ -267,13 +277,29 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
     pl.bt_bytes = (size_t)ceil_div((long long)p.N * pl.ldbt * 4, 256) * 256;
     bt_cycles = 8.0 * (double)p.K * p.N / 3400.0 + 2000.0;
   }
+  if (s.tma && !p.tma_ok) {  // aligned copies of the operands TMA cannot address
+    if (!p.a_tma) {
+      pl.pack_a = true;
+      pl.lda_p = ceil_div(p.K, 4) * 4;
+      pl.pack_a_bytes = (size_t)ceil_div((long long)p.M * pl.lda_p * 4, 256) * 256;
+      bt_cycles += 8.0 * (double)p.M * p.K / 3400.0 + 2000.0;
+    }
+    if (!p.b_tma) {
+      pl.pack_b = true;
+      pl.ldb_p = ceil_div(p.N, 4) * 4;
+      pl.pack_b_bytes = (size_t)ceil_div((long long)p.K * pl.ldb_p * 4, 256) * 256;
+      bt_cycles += 8.0 * (double)p.K * p.N / 3400.0 + 2000.0;
+    }
+  }
+  pl.pre_bytes = pl.bt_bytes + pl.pack_a_bytes + pl.pack_b_bytes;
   pl.main_tiles = (int)main;
   pl.split = split;
   pl.k_per_split = (int)(kt_per * s.BK);
   pl.group_m = std::min(16, pl.tiles_m);
   pl.ctas = (int)(main + slices);
-  pl.launches = (slices > 0 ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0);
-  pl.ws_bytes = pl.bt_bytes + (slices > 0 ? (size_t)part_bytes : 0);
+  pl.launches = (slices > 0 ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0) + (pl.pack_a ? 1 : 0) +
+                (pl.pack_b ? 1 : 0);
+  pl.ws_bytes = pl.pre_bytes + (slices > 0 ? (size_t)part_bytes : 0);
   pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce + bt_cycles;
   if (main + slices > 0x7fffffffLL) {  // grid too large for one launch
     pl.ctas = 0;
@@ -304,10 +330,10 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   const bool beta_nz = beta != 0.0f;
   best.cycles = std::numeric_limits<double>::infinity();
   const double ws_cap = 64.0 * 1024 * 1024;  // largest split-K workspace the plan may use
-  const size_t bt_cap = (size_t)2 << 30;       // largest B^T copy the plan may make
+  const size_t bt_cap = (size_t)2 << 30;  // largest pre-pass copies (B^T, packs) a plan makes
   auto consider = [&](const Plan &c) {
-    if ((double)(c.ws_bytes - c.bt_bytes) > ws_cap && force_split < 1) return;
-    if (c.bt_bytes > bt_cap) return;
+    if ((double)(c.ws_bytes - c.pre_bytes) > ws_cap && force_split < 1) return;
+    if (c.pre_bytes > bt_cap) return;
     if (c.cycles < best.cycles * 0.999) best = c;  // prefer earlier (simpler) on ties
   };
   const int v_lo = force_v >= 0 ? force_v : 0;
@@ -316,7 +342,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   for (int v = v_lo; v <= v_hi; ++v) {
     if (force_v < 0 && !kVariants[v].automatic) continue;
     if (trans && !kVariants[v].trans_ok) continue;
-    if (kVariants[v].tma && !p.tma_ok) continue;
+    if (kVariants[v].tma && !p.tma_ok && (p.transa || p.transb)) continue;
     if (kVariants[v].kpair && (!p.kpair_ok || (force_v < 0 && !p.b_kmajor))) continue;
     const VariantShape &s = kVariants[v];
     if (s.thin) {

@@ -26,7 +26,9 @@
  *   A, B and C are device pointers owned by the caller (any memory the GPU can address with
  *   a plain load: cudaMalloc, cudaMallocAsync, managed). The library keeps no pointer after
  *   the call returns. C must not overlap A or B.
- *   sgemm_f32 may allocate a split-K workspace (at most 64 MiB) with a stream-ordered
+ *   sgemm_f32 may allocate a workspace (split-K partial tiles, at most 64 MiB, plus aligned
+ *   copies of A and B when lda or ldb is not a multiple of 4 or a pointer is not 16-byte
+ *   aligned, at most 2 GiB) with a stream-ordered
  *   allocation on `stream` and free it on the same stream before returning. It comes from
  *   a memory pool the library creates per device, which keeps freed memory for reuse until
  *   the process exits. sgemm_f32_workspace_size() reports the size; sgemm_f32_ws() takes
@@ -214,9 +216,11 @@ int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha
  * several host threads) race on the array and give wrong results. Nothing in the array has
  * to start at zero: a call writes every workspace element before it reads it.
  *
- * Errors: as sgemm_f32, plus SGEMM_F32_ERR_SCRATCH_TOO_SMALL when the problem's split-K
- * plan needs more workspace than the array holds (sgemm_f32_workspace_size() reports the
- * need beforehand); nothing is launched in that case. */
+ * Errors: as sgemm_f32, plus SGEMM_F32_ERR_SCRATCH_TOO_SMALL when the problem's plan
+ * needs more workspace than the array holds (sgemm_f32_workspace_size() reports the need
+ * beforehand): split-K partial tiles, plus, when lda or ldb is not a multiple of 4 or A or
+ * B is not 16-byte aligned, the aligned copies of those operands that the plan makes
+ * (large unaligned problems therefore exceed it). Nothing is launched in that case. */
 int sgemm_f32_noalloc(int M, int N, int K, float alpha, const float *A, int lda,
                       const float *B, int ldb, float beta, float *C, int ldc,
                       cudaStream_t stream);

@@ -112,20 +112,35 @@ def test_plan_thin_shapes_use_thin_tiles_and_split_k():
     assert info["BN"] <= 16 and p["split"] > 1
 
 
+TMA_VARIANTS = (26, 30, 31, 32)  # TMA-fed configurations (aligned copies of other operands)
+
+
 def test_plan_workspace_formula():
-    """Workspace = one BM x BN float tile per K slice of every split tile."""
+    """Workspace = aligned copies of the operands a TMA-fed plan cannot address (rows of
+    ceil4(cols) floats, 256-byte rounded), then one BM x BN float tile per K slice of every
+    split tile. Launches = the copies + the GEMM + the split-K finish."""
+    def r256(x):
+        return -(-x // 256) * 256
+
     for shp in [(16, 4096, 4096), (4096, 16, 8192), (256, 256, 256), (1023, 1021, 4096),
-                (8192, 8192, 8192), (4097, 4097, 4097)]:
+                (8192, 8192, 8192), (4097, 4097, 4097), (4099, 3001, 777)]:
         M, N, K = shp
         p = _plan(M, N, K)
         info = sg.sgemm_f32_variant_info(p["variant"])
         tiles = -(-M // info["BM"]) * -(-N // info["BN"])
         split_tiles = tiles - p["main_tiles"]
+        pre, copies = 0, 0
+        if p["variant"] in TMA_VARIANTS:
+            if K % 4:
+                pre, copies = pre + r256(4 * M * (-(-K // 4) * 4)), copies + 1
+            if N % 4:
+                pre, copies = pre + r256(4 * K * (-(-N // 4) * 4)), copies + 1
         if p["split"] > 1:
-            assert split_tiles > 0 and p["launches"] == 2
-            assert p["ws_bytes"] == 4 * p["split"] * split_tiles * info["BM"] * info["BN"]
+            assert split_tiles > 0 and p["launches"] == 2 + copies
+            assert p["ws_bytes"] == pre + 4 * p["split"] * split_tiles * info["BM"] * info["BN"]
         else:
-            assert p["main_tiles"] == tiles and p["ws_bytes"] == 0 and p["launches"] == 1
+            assert p["main_tiles"] == tiles and p["ws_bytes"] == pre
+            assert p["launches"] == 1 + copies
 
 
 def test_plan_tail_split_keeps_whole_waves():

@@ -108,8 +108,6 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
-    if not aligned and variant in TMA_VARIANTS:
-        pytest.skip("the TMA-fed configuration needs aligned operands")
     for (M, N, K) in RAGGED:
         A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
         if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS:
@@ -187,13 +185,24 @@ def test_variant_count():
     assert sg.sgemm_f32_num_variants() == NUM_VARIANTS
 
 
-def test_tma_variant_refuses_unaligned():
+def test_tma_variants_on_unaligned_and_transposed_operands():
+    """A TMA-fed configuration packs row-major operands that TMA cannot address (odd ld,
+    misaligned pointer) into aligned copies and still meets the bound; it has no path for
+    transposed operands (-14). The K-paired configurations need an addressable A (-14)."""
     A, B, C = make_inputs(64, 64, 64, seed=12)
     dA, _ = to_device_view(A, 65, 1)
-    dB, _ = to_device_view(B)
+    dB, _ = to_device_view(B, 67, 3)
+    R, S = oracle.sgemm_f64(A, B, None, 1.0, 0.0)
+    for v in TMA_VARIANTS:
+        dC, _ = to_device_view(C)
+        assert sg.sgemm_f32_forced(64, 64, 64, 1.0, dA, 65, dB, 67, 0.0, dC, 64, v, 1) == 0
+        torch.cuda.synchronize()
+        assert_bound(dC.cpu().numpy(), R, S, 0.0, None, f"packed v{v}")
+        assert sg.sgemm_f32_ex_forced(1, 0, 64, 64, 64, 1.0, dA, 65, dB, 67, 0.0, dC, 64,
+                                      v, 1) == -14
     dC, _ = to_device_view(C)
-    for v in TMA_VARIANTS + KPAIR_VARIANTS:
-        assert sg.sgemm_f32_forced(64, 64, 64, 1.0, dA, 65, dB, 64, 0.0, dC, 64, v, 1) == -14
+    for v in KPAIR_VARIANTS:
+        assert sg.sgemm_f32_forced(64, 64, 64, 1.0, dA, 65, dB, 67, 0.0, dC, 64, v, 1) == -14
 
 
 def test_status_words_clear():

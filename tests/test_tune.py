@@ -15,8 +15,8 @@ def _empty_table():
 
 
 # flags of a row-major problem with 16-byte aligned A, B and lda, ldb multiples of 4
-# (TMA-able = 4, K-paired-able = 8) and beta != 0 (32)
-FLAGS_ALIGNED_BETA = 4 | 8 | 32
+# (TMA-able = 4, K-paired-able = 8, A and B TMA-addressable = 64, 128) and beta != 0 (32)
+FLAGS_ALIGNED_BETA = 4 | 8 | 32 | 64 | 128
 
 
 def test_load_applies_to_its_key_only(tmp_path):
