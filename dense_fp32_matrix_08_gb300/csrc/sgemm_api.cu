@@ -33,9 +33,13 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},
     VariantKernels{},  // thin-M and thin-N streaming kernels (sgemm_thin.cu)
     VariantKernels{},
+    VariantKernels{},  // k-major TMA-fed instances (sgemm_tma.cu)
+    VariantKernels{},
+    VariantKernels{},  // TMA-fed instances transposing A in the CTA (sgemm_tma.cu)
+    VariantKernels{},
 };
 static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
-                  kThinNVariant == 34 && kNumVariants == 35,
+                  kThinNVariant == 34 && kNumVariants == 39,
               "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
@@ -116,7 +120,8 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
                          (beta == 1.0f ? 4u : 0u) | (pr.transa ? 8u : 0u) |
                          (pr.transb ? 16u : 0u) | (pr.tma_ok ? 32u : 0u) |
                          (pr.kpair_ok ? 64u : 0u) | (pr.b_kmajor ? 128u : 0u) |
-                         (pr.a_tma ? 256u : 0u) | (pr.b_tma ? 512u : 0u);
+                         (pr.a_tma ? 256u : 0u) | (pr.b_tma ? 512u : 0u) |
+                         (pr.at_direct ? 1024u : 0u);
   for (int i = 0; i < kEntries; ++i) {
     const Entry &e = cache[i];
     if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
@@ -244,7 +249,13 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     char *wsb = reinterpret_cast<char *>(ws);
     const float *Ap = A, *Bp = B;
     long long ldap = pr.lda, ldbp = pr.ldb;
-    if (pl.pack_a) {
+    if (pl.at_a) {  // k-major instances read A^T
+      float *dst = reinterpret_cast<float *>(wsb + pl.bt_bytes);
+      cudaError_t te = launch_transpose_b(A, pr.lda, pr.M, pr.K, dst, pl.lda_p, num_sms, stream);
+      if (te != cudaSuccess) return (int)te;
+      Ap = dst;
+      ldap = pl.lda_p;
+    } else if (pl.pack_a) {
       float *dst = reinterpret_cast<float *>(wsb + pl.bt_bytes);
       const long long work = (long long)pr.M * ((pr.K + 3) / 4);
       pack_rows_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
@@ -304,12 +315,15 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   pr.b_kmajor = transb && ldb % 4 == 0 && aligned16(B);
   pr.a_tma = !transa && lda % 4 == 0 && aligned16(A) && A != nullptr;
   pr.b_tma = !transb && ldb % 4 == 0 && aligned16(B) && B != nullptr;
+  pr.at_direct = transa && lda % 4 == 0 && aligned16(A) && A != nullptr;
   int rc = (transa || transb) ? validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr)
                               : validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
   if (rc != 0) return rc;
   if (M == 0 || N == 0) return 0;
   if (force_v >= kNumVariants || force_v < -1) return kErrBadVariant;
-  if (force_v >= 0 && kVariants[force_v].tma && (transa || transb)) return kErrBadVariant;
+  if (force_v >= 0 && kVariants[force_v].tma && (transa || transb) &&
+      !(kVariants[force_v].at && pr.at_direct && !transb))
+    return kErrBadVariant;
   if (force_v >= 0 && kVariants[force_v].kpair && !pr.kpair_ok) return kErrBadVariant;
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
@@ -325,6 +339,9 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   // No candidate fitted (a forced configuration whose workspace exceeds the limits).
   if (pl.variant < 0 && alpha != 0.0f && K > 0) return force_v >= 0 ? kErrBadVariant
                                                                     : kErrWorkspace;
+  // A caller workspace that cannot hold the plan's A^T copy gets the twin configuration
+  // that transposes A in shared memory: the same tiles and k order, no copy.
+  if (ws_mode == 1 && pl.ws_bytes > ws_bytes) pl = without_at_copy(pr, pl);
   float *wsp = nullptr;
   if (pl.ws_bytes > 0) {
     if (ws_mode == 1) {
@@ -401,9 +418,6 @@ int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha
   Problem pr{M, N, K, lda, ldb, ldc, transa, transb};
   const int rc = validate_ex(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
   if (rc != 0) return rc;
-  if (variant >= 0 && variant < kNumVariants && (transa || transb) &&
-      !kVariants[variant].trans_ok)
-    return kErrBadVariant;
   return sgemm_entry(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, variant, split, 0, nullptr,
                      0, stream, transa, transb);
 }

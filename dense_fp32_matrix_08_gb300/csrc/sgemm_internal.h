@@ -37,7 +37,8 @@ cudaError_t thin_setup();
 cudaError_t launch_thin(bool thin_m, const thin::ThinParams &p, bool vec, cudaStream_t stream);
 
 // TMA-fed GEMM (sgemm_ffma_tma.cuh): one-time kernel attributes for the current device, and
-// a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb).
+// a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb); for
+// the k-major instances A is A^T (K x M, row stride lda).
 cudaError_t tma_setup();
 cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
                        const GemmParams &p, int ctas, int *status, cudaStream_t stream);

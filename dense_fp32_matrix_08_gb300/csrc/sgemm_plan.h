@@ -19,6 +19,8 @@ struct Problem {
   bool tma_ok = false;         // A, B 16-byte aligned with lda, ldb % 4 == 0 (TMA-fed kernel)
   bool a_tma = false;          // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
   bool b_tma = false;          // op(B) = B row-major, 16-byte aligned, ldb % 4 == 0
+  bool at_direct = false;      // op(A) = A_st^T with A_st (K x M) 16-byte aligned, lda % 4 == 0:
+                               // A_st is the k-major A the at variants read, no copy needed
   bool kpair_ok = false;       // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
   bool b_kmajor = false;       // op(B) = B_st^T with B_st 16-byte aligned, ldb % 4 == 0
 };
@@ -33,6 +35,9 @@ struct VariantShape {
   bool kpair = false;  // the K-paired TMA-fed kernel (sgemm_ffma_kpair.cuh): K-major B
   int inst = 0;        // TMA-fed kernels: instance index of the launcher (sgemm_tma.cu)
   int thin = 0;        // streaming kernels of sgemm_thin.cuh: 1 thin-M, 2 thin-N
+  bool at = false;     // TMA-fed kernel reading A k-major (A^T; copied first if row-major)
+  int twin = -1;       // at variants: the variant with the same tiles and arithmetic that
+                       // transposes A in shared memory instead (bitwise the same result)
 };
 
 // mode: 0 scalar FFMA, 1 FFMA2 with register broadcast, 2 FFMA2 with duplicated A in smem
@@ -84,6 +89,16 @@ constexpr VariantShape kVariants[] = {
     // (4 rows x 16 columns per thread, 1 CTA/SM). BK is the k batch of the streamed loads.
     {16, 256, 8, 256, 16, 4, 1, 2, 1, 0, 0.65, false, false, false, false, 0, 1},
     {1024, 16, 8, 256, 4, 16, 1, 1, 1, 0, 0.65, false, false, false, false, 0, 2},
+    // 35, 36: the TMA-fed 128 x 96 and 128 x 128 shapes reading A k-major: A is copied to
+    // A^T first, and the A tile arrives as [32 k][128 m] like the B tile. Their math loop
+    // sustains ~9% more than 30 / 31 (measured 69.6 against 63.7 TFLOP/s at 8192^3).
+    {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1), 1.06, true, false, true, false, 4, 0, true, 37},
+    {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 1.04, true, false, true, false, 5, 0, true, 38},
+    // 37, 38: the same two shapes reading A as stored and transposing each A tile in shared
+    // memory (no workspace, no pre-pass; ~3% slower than 35 / 36); 128 x 128 with 2 stages
+    // to fit 2 CTAs/SM
+    {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1) + 16384, 1.028, true, false, true, false, 6},
+    {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1) + 16384, 1.03, true, false, true, false, 7},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;
@@ -113,6 +128,8 @@ struct Plan {
   bool pack_a = false, pack_b = false;
   long long lda_p = 0, ldb_p = 0;
   size_t pack_a_bytes = 0, pack_b_bytes = 0;
+  // k-major TMA-fed variants: A^T (K x ldat) made by a transpose pre-pass (in pack_a_bytes)
+  bool at_a = false;
   size_t pre_bytes = 0;
   double cycles = 0;    // modelled cost
 };
@@ -277,8 +294,14 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
     pl.bt_bytes = (size_t)ceil_div((long long)p.N * pl.ldbt * 4, 256) * 256;
     bt_cycles = 8.0 * (double)p.K * p.N / 3400.0 + 2000.0;
   }
+  if (s.at && !p.at_direct) {  // A^T first: M K floats read and written, one launch
+    pl.at_a = true;
+    pl.lda_p = ceil_div(p.M, 4) * 4;
+    pl.pack_a_bytes = (size_t)ceil_div((long long)p.K * pl.lda_p * 4, 256) * 256;
+    bt_cycles += 8.0 * (double)p.M * p.K / 3400.0 + 2000.0;
+  }
   if (s.tma && !p.tma_ok) {  // aligned copies of the operands TMA cannot address
-    if (!p.a_tma) {
+    if (!p.a_tma && !s.at) {
       pl.pack_a = true;
       pl.lda_p = ceil_div(p.K, 4) * 4;
       pl.pack_a_bytes = (size_t)ceil_div((long long)p.M * pl.lda_p * 4, 256) * 256;
@@ -297,8 +320,8 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   pl.k_per_split = (int)(kt_per * s.BK);
   pl.group_m = std::min(16, pl.tiles_m);
   pl.ctas = (int)(main + slices);
-  pl.launches = (slices > 0 ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0) + (pl.pack_a ? 1 : 0) +
-                (pl.pack_b ? 1 : 0);
+  pl.launches = (slices > 0 ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0) +
+                (pl.pack_a || pl.at_a ? 1 : 0) + (pl.pack_b ? 1 : 0);
   pl.ws_bytes = pl.pre_bytes + (slices > 0 ? (size_t)part_bytes : 0);
   pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce + bt_cycles;
   if (main + slices > 0x7fffffffLL) {  // grid too large for one launch
@@ -306,6 +329,25 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
     pl.cycles = std::numeric_limits<double>::infinity();
   }
   return pl;
+}
+
+// The same plan with an at variant replaced by its twin, which transposes A in shared
+// memory instead of reading a transposed copy: identical tiles, slices and k order (so
+// bitwise the same result), without the A^T workspace or its launch. Only for an A that
+// TMA can read as stored; otherwise the plan is returned unchanged.
+inline Plan without_at_copy(const Problem &p, const Plan &pl) {
+  if (pl.variant < 0 || !pl.at_a || !p.a_tma) return pl;
+  const VariantShape &s = kVariants[pl.variant];
+  if (s.twin < 0) return pl;
+  Plan t = pl;
+  t.variant = s.twin;
+  t.at_a = false;
+  t.pre_bytes -= pl.pack_a_bytes;
+  t.ws_bytes -= pl.pack_a_bytes;
+  t.pack_a_bytes = 0;
+  t.lda_p = 0;
+  t.launches -= 1;
+  return t;
 }
 
 // Choose the tile configuration and the split-K layout. Candidates per variant: no split;
@@ -341,8 +383,11 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   const bool trans = p.transa || p.transb;
   for (int v = v_lo; v <= v_hi; ++v) {
     if (force_v < 0 && !kVariants[v].automatic) continue;
-    if (trans && !kVariants[v].trans_ok) continue;
-    if (kVariants[v].tma && !p.tma_ok && (p.transa || p.transb)) continue;
+    const bool at_path = kVariants[v].at && p.at_direct && !p.transb;  // A_st is A^T
+    if (trans && !kVariants[v].trans_ok && !at_path) continue;
+    if (kVariants[v].tma && !p.tma_ok && (p.transa || p.transb) &&
+        !(kVariants[v].at && p.at_direct && !p.transb))
+      continue;
     if (kVariants[v].kpair && (!p.kpair_ok || (force_v < 0 && !p.b_kmajor))) continue;
     const VariantShape &s = kVariants[v];
     if (s.thin) {

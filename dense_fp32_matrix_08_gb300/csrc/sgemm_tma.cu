@@ -14,7 +14,11 @@ using Tma0 = tma::TmaCfg<128, 16, 3, 2, true>;   // 128 x 128, 8 x 16 threads, 2
 using Tma1 = tma::TmaCfg<96, 12, 2, 3, false>;   // 128 x 96, 8 x 12 threads, 3 CTAs/SM
 using Tma2 = tma::TmaCfg<128, 16, 3, 2, false>;  // Tma0 without A double-buffering
 using Tma3 = tma::TmaCfg<64, 8, 2, 4, false>;    // 128 x 64, 8 x 8 threads, 4 CTAs/SM
-constexpr int kInstances = 4;
+using Tma4 = tma::TmaCfg<96, 12, 2, 3, false, 1>;   // Tma1 on k-major A (A^T)
+using Tma5 = tma::TmaCfg<128, 16, 3, 2, false, 1>;  // Tma2 on k-major A (A^T)
+using Tma6 = tma::TmaCfg<96, 12, 2, 3, false, 2>;   // Tma1, A transposed in the CTA
+using Tma7 = tma::TmaCfg<128, 16, 2, 2, false, 2>;  // 128 x 128, 2 stages, A transposed
+constexpr int kInstances = 8;
 
 std::once_flag g_once[64];
 cudaError_t g_err[64];
@@ -29,7 +33,11 @@ template <class Cfg>
 cudaError_t launch(const float *A, long long lda, const float *B, long long ldb,
                    const GemmParams &p, int ctas, int *status, cudaStream_t stream) {
   CUtensorMap map_a, map_b;
-  if (!encode_map_2d(&map_a, A, p.M, p.K, lda, Cfg::BK, Cfg::BM, true) ||
+  // k-major A (AT): A points at A^T, K x M with row stride lda; [32 k][128 m] boxes
+  const bool ok_a = Cfg::AMODE == 1
+                        ? encode_map_2d(&map_a, A, p.K, p.M, lda, Cfg::BM, Cfg::BK, false)
+                        : encode_map_2d(&map_a, A, p.M, p.K, lda, Cfg::BK, Cfg::BM, true);
+  if (!ok_a ||
       !encode_map_2d(&map_b, B, p.K, p.N, ldb, Cfg::BN, Cfg::BK, false))
     return cudaErrorInvalidValue;
   tma::sgemm_tma_kernel<Cfg><<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(map_a, map_b, p,
@@ -49,6 +57,10 @@ cudaError_t tma_setup() {
     if (err == cudaSuccess) err = set_smem<Tma1>();
     if (err == cudaSuccess) err = set_smem<Tma2>();
     if (err == cudaSuccess) err = set_smem<Tma3>();
+    if (err == cudaSuccess) err = set_smem<Tma4>();
+    if (err == cudaSuccess) err = set_smem<Tma5>();
+    if (err == cudaSuccess) err = set_smem<Tma6>();
+    if (err == cudaSuccess) err = set_smem<Tma7>();
     g_err[dev] = err;
   });
   return g_err[dev];
@@ -56,12 +68,16 @@ cudaError_t tma_setup() {
 
 cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
                        const GemmParams &p, int ctas, int *status, cudaStream_t stream) {
-  static_assert(kInstances == 4, "instance table");
+  static_assert(kInstances == 8, "instance table");
   switch (inst) {
     case 0: return launch<Tma0>(A, lda, B, ldb, p, ctas, status, stream);
     case 1: return launch<Tma1>(A, lda, B, ldb, p, ctas, status, stream);
     case 2: return launch<Tma2>(A, lda, B, ldb, p, ctas, status, stream);
     case 3: return launch<Tma3>(A, lda, B, ldb, p, ctas, status, stream);
+    case 4: return launch<Tma4>(A, lda, B, ldb, p, ctas, status, stream);
+    case 5: return launch<Tma5>(A, lda, B, ldb, p, ctas, status, stream);
+    case 6: return launch<Tma6>(A, lda, B, ldb, p, ctas, status, stream);
+    case 7: return launch<Tma7>(A, lda, B, ldb, p, ctas, status, stream);
     default: return cudaErrorInvalidValue;
   }
 }

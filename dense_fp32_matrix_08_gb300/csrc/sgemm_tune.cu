@@ -25,7 +25,8 @@ namespace {
 
 struct TuneKey {
   int num_sms, M, N, K;
-  unsigned flags;  // transa, transb, tma_ok, kpair_ok, b_kmajor, beta != 0, a_tma, b_tma
+  unsigned flags;  // transa, transb, tma_ok, kpair_ok, b_kmajor, beta != 0, a_tma, b_tma,
+                   // at_direct
   bool operator==(const TuneKey &o) const {
     return num_sms == o.num_sms && M == o.M && N == o.N && K == o.K && flags == o.flags;
   }
@@ -43,7 +44,7 @@ std::vector<TuneEntry> g_table;
 unsigned key_flags(const Problem &pr, bool beta_nz) {
   return (pr.transa ? 1u : 0u) | (pr.transb ? 2u : 0u) | (pr.tma_ok ? 4u : 0u) |
          (pr.kpair_ok ? 8u : 0u) | (pr.b_kmajor ? 16u : 0u) | (beta_nz ? 32u : 0u) |
-         (pr.a_tma ? 64u : 0u) | (pr.b_tma ? 128u : 0u);
+         (pr.a_tma ? 64u : 0u) | (pr.b_tma ? 128u : 0u) | (pr.at_direct ? 256u : 0u);
 }
 
 void insert(const TuneEntry &e) {
@@ -95,6 +96,7 @@ int sgemm_f32_autotune(int transa, int transb, int M, int N, int K, float alpha,
   pr.b_kmajor = transb && ldb % 4 == 0 && aligned16(B);
   pr.a_tma = !transa && lda % 4 == 0 && aligned16(A);
   pr.b_tma = !transb && ldb % 4 == 0 && aligned16(B);
+  pr.at_direct = transa && lda % 4 == 0 && aligned16(A);
   if (reps <= 0) reps = 3;
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
@@ -214,7 +216,7 @@ int sgemm_f32_tune_load(const char *path) {
     if (std::sscanf(line, "%d %d %d %d %u %d %d %lf", &x.key.num_sms, &x.key.M, &x.key.N,
                     &x.key.K, &x.key.flags, &x.variant, &x.split, &t) != 8 ||
         x.key.num_sms <= 0 || x.key.M <= 0 || x.key.N <= 0 || x.key.K <= 0 ||
-        x.key.flags > 255u || x.variant < 0 || x.variant >= kNumVariants || x.split < -64 ||
+        x.key.flags > 511u || x.variant < 0 || x.variant >= kNumVariants || x.split < -64 ||
         x.split > 64) {
       ++bad;
       continue;

@@ -179,8 +179,12 @@ int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
 
 /* sgemm_f32_ex with the plan forced (variant and split as in sgemm_f32_forced). Returns
  * -14 also when the forced configuration has no path for these transpose flags or this
- * alignment: the TMA-fed configuration needs transa = transb = 0; the K-paired ones need
- * transa = 0 and A 16-byte aligned with lda a multiple of 4. */
+ * alignment:
+ *   - the TMA-fed configurations need transb = 0, and transa = 0, except the k-major ones
+ *     (sgemm_f32_variant_info: 35, 36), which also take transa = 1 with A_st 16-byte
+ *     aligned and lda a multiple of 4 (A_st is then read directly);
+ *   - the K-paired ones need transa = 0 and A 16-byte aligned with lda a multiple of 4;
+ *   - the copy-fed ones carry transposed-operand paths only in configurations 2, 3, 4, 16. */
 int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha,
                         const float *A, int lda, const float *B, int ldb, float beta, float *C,
                         int ldc, int variant, int split, cudaStream_t stream);
@@ -216,8 +220,14 @@ int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha
  * several host threads) race on the array and give wrong results. Nothing in the array has
  * to start at zero: a call writes every workspace element before it reads it.
  *
- * Errors: as sgemm_f32, plus SGEMM_F32_ERR_SCRATCH_TOO_SMALL when the problem's plan
- * needs more workspace than the array holds (sgemm_f32_workspace_size() reports the need
+ * Workspace: when the plan reads a transposed copy of A (the k-major TMA-fed
+ * configurations) and that copy does not fit, the call runs the twin configuration that
+ * transposes A in shared memory instead. The tiles, slices and k order are the same, so
+ * the result is still bitwise sgemm_f32's. sgemm_f32_ws does the same with a caller
+ * workspace that is too small for the copy.
+ *
+ * Errors: as sgemm_f32, plus SGEMM_F32_ERR_SCRATCH_TOO_SMALL when the rest of the plan's
+ * workspace does not fit the array (sgemm_f32_workspace_size() reports the full need
  * beforehand): split-K partial tiles, plus, when lda or ldb is not a multiple of 4 or A or
  * B is not 16-byte aligned, the aligned copies of those operands that the plan makes
  * (large unaligned problems therefore exceed it). Nothing is launched in that case. */

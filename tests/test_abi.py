@@ -100,7 +100,8 @@ def test_plan_headline_uses_large_tiles():
     p = _plan(8192, 8192, 8192)
     info = sg.sgemm_f32_variant_info(p["variant"])
     assert info["TM"] * info["TN"] >= 64
-    assert p["launches"] == (2 if p["split"] > 1 else 1)
+    pre = 1 if p["variant"] in AT_VARIANTS else 0  # the A^T copy
+    assert p["launches"] == pre + (2 if p["split"] > 1 else 1)
 
 
 def test_plan_thin_shapes_use_thin_tiles_and_split_k():
@@ -112,13 +113,15 @@ def test_plan_thin_shapes_use_thin_tiles_and_split_k():
     assert info["BN"] <= 16 and p["split"] > 1
 
 
-TMA_VARIANTS = (26, 30, 31, 32)  # TMA-fed configurations (aligned copies of other operands)
+TMA_VARIANTS = (26, 30, 31, 32, 37, 38)  # TMA-fed, A as stored (aligned copies if needed)
+AT_VARIANTS = (35, 36)  # TMA-fed, reading a transposed copy of A (B copied aligned if needed)
 
 
 def test_plan_workspace_formula():
-    """Workspace = aligned copies of the operands a TMA-fed plan cannot address (rows of
-    ceil4(cols) floats, 256-byte rounded), then one BM x BN float tile per K slice of every
-    split tile. Launches = the copies + the GEMM + the split-K finish."""
+    """Workspace = the A^T copy of a k-major plan (K rows of ceil4(M) floats) and aligned
+    copies of the operands a TMA-fed plan cannot address (rows of ceil4(cols) floats), each
+    256-byte rounded, then one BM x BN float tile per K slice of every split tile.
+    Launches = the copies + the GEMM + the split-K finish."""
     def r256(x):
         return -(-x // 256) * 256
 
@@ -130,11 +133,12 @@ def test_plan_workspace_formula():
         tiles = -(-M // info["BM"]) * -(-N // info["BN"])
         split_tiles = tiles - p["main_tiles"]
         pre, copies = 0, 0
-        if p["variant"] in TMA_VARIANTS:
-            if K % 4:
-                pre, copies = pre + r256(4 * M * (-(-K // 4) * 4)), copies + 1
-            if N % 4:
-                pre, copies = pre + r256(4 * K * (-(-N // 4) * 4)), copies + 1
+        if p["variant"] in AT_VARIANTS:
+            pre, copies = pre + r256(4 * K * (-(-M // 4) * 4)), copies + 1
+        if p["variant"] in TMA_VARIANTS and K % 4:
+            pre, copies = pre + r256(4 * M * (-(-K // 4) * 4)), copies + 1
+        if p["variant"] in TMA_VARIANTS + AT_VARIANTS and N % 4:
+            pre, copies = pre + r256(4 * K * (-(-N // 4) * 4)), copies + 1
         if p["split"] > 1:
             assert split_tiles > 0 and p["launches"] == 2 + copies
             assert p["ws_bytes"] == pre + 4 * p["split"] * split_tiles * info["BM"] * info["BN"]

@@ -118,3 +118,24 @@ def test_colmajor_against_oracle(transa, transb):
     assert np.all(np.isnan(dC.cpu().numpy()[:, m:]))  # padding rows untouched
     R, S = oracle.sgemm_f64(opA, opB, C, 2.0, 0.25)
     assert_bound(out, R, S, 0.25, C.numpy(), f"colmajor T{transa}{transb}")
+
+
+@pytest.mark.parametrize("variant", [35, 36])
+def test_k_major_tma_reads_transposed_a_directly(variant):
+    """With op(A) = A_st^T and A_st aligned, the k-major TMA-fed configurations read A_st as
+    the A^T they need (no copy): parity, and the same result bits as their row-major run."""
+    M, N, K = 700, 520, 300
+    opA, opB, C = make_inputs(M, N, K, seed=variant)
+    At = opA.t().contiguous()
+    dC1, dC2 = C.cuda(), C.cuda()
+    assert sg.sgemm_f32_ex_forced(1, 0, M, N, K, 1.0, At.cuda(), M, opB.cuda(), N, 0.5, dC1, N,
+                                  variant, 0) == 0
+    assert sg.sgemm_f32_forced(M, N, K, 1.0, opA.cuda(), K, opB.cuda(), N, 0.5, dC2, N,
+                               variant, 0) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(dC1, dC2)
+    R, S = oracle.sgemm_f64(opA, opB, C, 1.0, 0.5)
+    assert_bound(dC1.cpu().numpy(), R, S, 0.5, C.numpy(), f"A^T direct v{variant}")
+    # no path for a transposed B
+    assert sg.sgemm_f32_ex_forced(1, 1, M, N, K, 1.0, At.cuda(), M, opB.t().contiguous().cuda(),
+                                  K, 0.5, dC1, N, variant, 0) == -14

@@ -76,8 +76,10 @@ def test_noalloc_matches_sgemm_f32_twice(M, N, K, alpha, beta, seed):
 def test_noalloc_refuses_problems_beyond_the_scratch():
     import dense_fp32_matrix_08_gb300 as sg
 
+    # Odd leading dimensions: the plan's aligned operand copies cannot be dropped (only an
+    # A^T copy has a shared-memory twin), so a large enough problem exceeds the scratch.
     big = None
-    for n in (3000, 3200, 3600, 4000, 2900, 6000):
+    for n in (3001, 3201, 3601, 4001, 6001):
         p = sg.sgemm_f32_plan(n, n, n, n, n, n, 1.0, 1.0, 0)
         if p["ws_bytes"] > SCRATCH_BYTES:
             big = n
@@ -107,3 +109,26 @@ def test_noalloc_without_scratch_need():
     torch.cuda.synchronize()
     R, S = oracle.sgemm_f64(A, B, None, 1.0, 0.0)
     assert_bound(dC.cpu().numpy(), R, S, 0.0, None, "noalloc small")
+
+
+def test_noalloc_twin_is_bitwise_sgemm_f32():
+    """A large aligned problem whose plan reads a transposed copy of A (more workspace than
+    the scratch) runs through the twin configuration that transposes A in shared memory:
+    the same tiles, slices and k order, so the result is bitwise sgemm_f32's."""
+    import dense_fp32_matrix_08_gb300 as sg
+
+    n = 3072
+    p = sg.sgemm_f32_plan(n, n, n, n, n, n, 1.0, 0.5, 0)
+    if p["ws_bytes"] <= SCRATCH_BYTES:
+        pytest.skip("the plan for this shape fits the scratch on this device")
+    A, B, C = make_inputs(n, n, n, seed=45)
+    dA, dB = A.cuda(), B.cuda()
+    ref = C.cuda()
+    out = C.cuda()
+    assert sg.sgemm_f32(n, n, n, 1.0, dA, n, dB, n, 0.5, ref, n) == 0
+    assert sg.sgemm_f32_noalloc(n, n, n, 1.0, dA, n, dB, n, 0.5, out, n) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    rows = np.array([0, 1, 1535, n - 1])
+    R, S = oracle.sgemm_f64_rows(A, B, C, 1.0, 0.5, rows)
+    assert_bound(out.cpu().numpy()[rows], R, S, 0.5, C.numpy()[rows], "noalloc twin")
