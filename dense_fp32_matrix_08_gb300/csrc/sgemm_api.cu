@@ -37,9 +37,11 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},
     VariantKernels{},  // TMA-fed instances transposing A in the CTA (sgemm_tma.cu)
     VariantKernels{},
+    VariantKernels{},  // more k-major TMA-fed instances (sgemm_tma.cu)
+    VariantKernels{},
 };
 static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
-                  kThinNVariant == 34 && kNumVariants == 39,
+                  kThinNVariant == 34 && kNumVariants == 41,
               "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).

@@ -99,6 +99,9 @@ constexpr VariantShape kVariants[] = {
     // to fit 2 CTAs/SM
     {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1) + 16384, 1.028, true, false, true, false, 6},
     {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1) + 16384, 1.03, true, false, true, false, 7},
+    // 39, 40: k-major A, 128 x 64 at 4 CTAs/SM and 128 x 128 with 2 stages
+    {128, 64, 32, 128, 8, 8, 2, 4, 1, smem_of(128, 64, 32, 2, 1), 1.055, false, false, true, false, 8, 0, true},
+    {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1), 1.0, false, false, true, false, 9, 0, true},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;

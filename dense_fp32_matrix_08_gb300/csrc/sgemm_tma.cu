@@ -18,7 +18,9 @@ using Tma4 = tma::TmaCfg<96, 12, 2, 3, false, 1>;   // Tma1 on k-major A (A^T)
 using Tma5 = tma::TmaCfg<128, 16, 3, 2, false, 1>;  // Tma2 on k-major A (A^T)
 using Tma6 = tma::TmaCfg<96, 12, 2, 3, false, 2>;   // Tma1, A transposed in the CTA
 using Tma7 = tma::TmaCfg<128, 16, 2, 2, false, 2>;  // 128 x 128, 2 stages, A transposed
-constexpr int kInstances = 8;
+using Tma8 = tma::TmaCfg<64, 8, 2, 4, false, 1>;    // 128 x 64 on k-major A, 4 CTAs/SM
+using Tma9 = tma::TmaCfg<128, 16, 2, 2, false, 1>;  // 128 x 128 on k-major A, 2 stages
+constexpr int kInstances = 10;
 
 std::once_flag g_once[64];
 cudaError_t g_err[64];
@@ -61,6 +63,8 @@ cudaError_t tma_setup() {
     if (err == cudaSuccess) err = set_smem<Tma5>();
     if (err == cudaSuccess) err = set_smem<Tma6>();
     if (err == cudaSuccess) err = set_smem<Tma7>();
+    if (err == cudaSuccess) err = set_smem<Tma8>();
+    if (err == cudaSuccess) err = set_smem<Tma9>();
     g_err[dev] = err;
   });
   return g_err[dev];
@@ -68,7 +72,7 @@ cudaError_t tma_setup() {
 
 cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
                        const GemmParams &p, int ctas, int *status, cudaStream_t stream) {
-  static_assert(kInstances == 8, "instance table");
+  static_assert(kInstances == 10, "instance table");
   switch (inst) {
     case 0: return launch<Tma0>(A, lda, B, ldb, p, ctas, status, stream);
     case 1: return launch<Tma1>(A, lda, B, ldb, p, ctas, status, stream);
@@ -78,6 +82,8 @@ cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, 
     case 5: return launch<Tma5>(A, lda, B, ldb, p, ctas, status, stream);
     case 6: return launch<Tma6>(A, lda, B, ldb, p, ctas, status, stream);
     case 7: return launch<Tma7>(A, lda, B, ldb, p, ctas, status, stream);
+    case 8: return launch<Tma8>(A, lda, B, ldb, p, ctas, status, stream);
+    case 9: return launch<Tma9>(A, lda, B, ldb, p, ctas, status, stream);
     default: return cudaErrorInvalidValue;
   }
 }

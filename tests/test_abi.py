@@ -114,7 +114,7 @@ def test_plan_thin_shapes_use_thin_tiles_and_split_k():
 
 
 TMA_VARIANTS = (26, 30, 31, 32, 37, 38)  # TMA-fed, A as stored (aligned copies if needed)
-AT_VARIANTS = (35, 36)  # TMA-fed, reading a transposed copy of A (B copied aligned if needed)
+AT_VARIANTS = (35, 36, 39, 40)  # TMA-fed, reading a transposed copy of A (B copied if needed)
 
 
 def test_plan_workspace_formula():

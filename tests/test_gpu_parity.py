@@ -15,8 +15,8 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 39  # compiled tile configurations; checked against the library below
-TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38)  # every TMA-fed instance
+NUM_VARIANTS = 41  # compiled tile configurations; checked against the library below
+TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
 
