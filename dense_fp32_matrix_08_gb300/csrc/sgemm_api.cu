@@ -39,9 +39,10 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},
     VariantKernels{},  // more k-major TMA-fed instances (sgemm_tma.cu)
     VariantKernels{},
+    VariantKernels{},  // TMA-fed thin-M with cluster reduction (sgemm_thin.cu)
 };
 static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
-                  kThinNVariant == 34 && kNumVariants == 41,
+                  kThinNVariant == 34 && kThinTmaVariant == 41 && kNumVariants == 42,
               "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
@@ -159,6 +160,16 @@ static int grid_for_stream_kernel(long long work_items, int num_sms) {
   return (int)std::max<long long>(1, std::min(blocks, cap));
 }
 
+// Launch shape of the split-K finish: small jobs (a few thousand float4 outputs, as for
+// thin problems) in 64-thread blocks so that they spread over every SM instead of a few
+// large blocks; large jobs in 256-thread blocks, at most 8 per SM, grid-stride.
+static void reduce_shape(long long work_items, int num_sms, int *grid, int *block) {
+  *block = work_items >= (long long)num_sms * 512 ? 256 : 64;
+  const long long blocks = (work_items + *block - 1) / *block;
+  const long long cap = (long long)num_sms * (2048 / *block);
+  *grid = (int)std::max<long long>(1, std::min(blocks, cap));
+}
+
 // Enqueue the whole computation for a validated, non-empty problem.
 static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
                const float *B, float beta, float *C, float *ws, int num_sms,
@@ -191,16 +202,24 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     tp.tiles_m = pl.tiles_m;
     tp.tiles_n = pl.tiles_n;
     tp.vec_c = vec_c ? 1 : 0;
-    // 128-bit loads of the streamed operand: B rows (thin-M) or A rows (thin-N)
-    const bool vec = vs.thin == 1 ? (pr.ldb % 4 == 0 && aligned16(B))
-                                  : (pr.lda % 4 == 0 && aligned16(A));
-    cudaError_t te = launch_thin(vs.thin == 1, tp, vec, stream);
+    cudaError_t te;
+    int parts = pl.split;  // partial tiles per C tile for the reduce kernel
+    if (vs.thin == 3) {
+      te = launch_thin_m_tma(tp, status_word(), stream);
+    } else {
+      // 128-bit loads of the streamed operand: B rows (thin-M) or A rows (thin-N)
+      const bool vec = vs.thin == 1 ? (pr.ldb % 4 == 0 && aligned16(B))
+                                    : (pr.lda % 4 == 0 && aligned16(A));
+      te = launch_thin(vs.thin == 1, tp, vec, stream);
+    }
     if (te != cudaSuccess) return (int)te;
-    if (pl.split > 1) {
+    if (parts > 1) {
       const long long tiles = (long long)pl.tiles_m * pl.tiles_n;
       const long long work = tiles * vs.BM * (vs.BN / 4);
-      tail_reduce_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
-          ws, 0, (int)tiles, pl.split, vs.BM, vs.BN, pl.tiles_m, pl.tiles_n, 1, pr.M, pr.N,
+      int rgrid = 1, rblock = 256;
+      reduce_shape(work, num_sms, &rgrid, &rblock);
+      tail_reduce_kernel<<<rgrid, rblock, 0, stream>>>(
+          ws, 0, (int)tiles, parts, vs.BM, vs.BN, pl.tiles_m, pl.tiles_n, 1, pr.M, pr.N,
           alpha, beta, C, pr.ldc, vec_c ? 1 : 0);
       te = cudaGetLastError();
     }
@@ -296,7 +315,9 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   const long long tail_tiles = (long long)pl.tiles_m * pl.tiles_n - pl.main_tiles;
   if (tail_tiles > 0) {
     const long long work = (long long)tail_tiles * vs.BM * (vs.BN / 4);
-    tail_reduce_kernel<<<grid_for_stream_kernel(work, num_sms), 256, 0, stream>>>(
+    int rgrid = 1, rblock = 256;
+    reduce_shape(work, num_sms, &rgrid, &rblock);
+    tail_reduce_kernel<<<rgrid, rblock, 0, stream>>>(
         ws, pl.main_tiles, (int)tail_tiles, pl.split, vs.BM, vs.BN, pl.tiles_m, pl.tiles_n,
         pl.group_m, pr.M, pr.N, alpha, beta, C, pr.ldc, vec_c ? 1 : 0);
     e = cudaGetLastError();

@@ -82,8 +82,23 @@ __global__ void tail_reduce_kernel(const float *__restrict__ ws, int main_tiles,
     const int col = tn * BN + c4;
     if (row >= M || col >= N) continue;
     const float *src = ws + (long long)t * split * tile_elems + (long long)r * BN + c4;
+    // Slices are added in ascending order; their loads are issued four at a time, so a
+    // thread waits for one memory latency per four slices instead of one per slice.
     float4 s = *reinterpret_cast<const float4 *>(src);
-    for (int k = 1; k < split; ++k) {
+    int k = 1;
+    for (; k + 4 <= split; k += 4) {
+      float4 q[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) q[u] = *reinterpret_cast<const float4 *>(src + (k + u) * tile_elems);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        s.x += q[u].x;
+        s.y += q[u].y;
+        s.z += q[u].z;
+        s.w += q[u].w;
+      }
+    }
+    for (; k < split; ++k) {
       const float4 q = *reinterpret_cast<const float4 *>(src + k * tile_elems);
       s.x += q.x;
       s.y += q.y;

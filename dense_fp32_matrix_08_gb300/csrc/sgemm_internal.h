@@ -35,6 +35,9 @@ struct ThinParams;
 // of the streamed operand allowed).
 cudaError_t thin_setup();
 cudaError_t launch_thin(bool thin_m, const thin::ThinParams &p, bool vec, cudaStream_t stream);
+// TMA-fed thin-M kernel (sgemm_thin_tma.cuh): p.split CTAs along K, p.k_per_split a
+// multiple of 8 and at most 1024; B TMA-addressable.
+cudaError_t launch_thin_m_tma(const thin::ThinParams &p, int *status, cudaStream_t stream);
 
 // TMA-fed GEMM (sgemm_ffma_tma.cuh): one-time kernel attributes for the current device, and
 // a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb); for

@@ -34,7 +34,8 @@ struct VariantShape {
   bool tma = false;  // the TMA-fed kernel (sgemm_ffma_tma.cuh), aligned row-major operands only
   bool kpair = false;  // the K-paired TMA-fed kernel (sgemm_ffma_kpair.cuh): K-major B
   int inst = 0;        // TMA-fed kernels: instance index of the launcher (sgemm_tma.cu)
-  int thin = 0;        // streaming kernels of sgemm_thin.cuh: 1 thin-M, 2 thin-N
+  int thin = 0;        // streaming kernels: 1 thin-M, 2 thin-N (sgemm_thin.cuh), 3 TMA-fed
+                       // thin-M (sgemm_thin_tma.cuh)
   bool at = false;     // TMA-fed kernel reading A k-major (A^T; copied first if row-major)
   int twin = -1;       // at variants: the variant with the same tiles and arithmetic that
                        // transposes A in shared memory instead (bitwise the same result)
@@ -67,7 +68,7 @@ constexpr VariantShape kVariants[] = {
     {128, 256, 16, 256, 4, 32, 4, 1, 1, smem_of(128, 256, 16, 4, 1), 0.80, false, false},
     {128, 128, 16, 128, 4, 32, 3, 2, 1, smem_of(128, 128, 16, 3, 1), 0.80, false, false},
     {16, 512, 16, 128, 8, 8, 3, 2, 1, smem_of(16, 512, 16, 3, 1), 0.60, false, false},
-    {128, 16, 32, 128, 4, 4, 4, 3, 0, smem_of(128, 16, 32, 4, 0), 0.50, false, false},
+    {128, 16, 32, 128, 4, 4, 4, 3, 0, smem_of(128, 16, 32, 4, 0), 0.55, true, false},
     {128, 128, 16, 128, 8, 16, 4, 2, 1, smem_of(128, 128, 16, 4, 1), 0.80, false, false},
     {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 0.80, false, false},
     {128, 128, 8, 128, 8, 16, 6, 2, 1, smem_of(128, 128, 8, 6, 1), 0.80, false, false},
@@ -102,6 +103,9 @@ constexpr VariantShape kVariants[] = {
     // 39, 40: k-major A, 128 x 64 at 4 CTAs/SM and 128 x 128 with 2 stages
     {128, 64, 32, 128, 8, 8, 2, 4, 1, smem_of(128, 64, 32, 2, 1), 1.055, false, false, true, false, 8, 0, true},
     {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1), 1.0, false, false, true, false, 9, 0, true},
+    // 41: TMA-fed thin-M, 16 x 256 C tiles, 8 warps each streaming its own 8-k chunks of B
+    // through 2 private stages, K slices reduced by the split-K finish (1 CTA/SM)
+    {16, 256, 8, 256, 16, 8, 2, 1, 1, 0, 0.7, true, false, false, false, 0, 3},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;
@@ -109,6 +113,7 @@ constexpr int kFirstKpairVariant = 27;
 constexpr int kThinMVariant = 33, kThinNVariant = 34;
 constexpr int kThinMaxDim = 64;  // thin kernels considered for M (thin-M) or N (thin-N) <= this
 constexpr int kThinMKmax = 512, kThinNKmax = 2048;  // K slice bounds (shared memory)
+constexpr int kThinTmaVariant = 41, kThinTmaKmax = 1024;
 static_assert(kVariants[kTmaVariant].tma, "TMA variant index");
 static_assert(kVariants[kFirstKpairVariant].kpair, "K-paired variant index");
 
@@ -150,9 +155,10 @@ inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool bet
   pl.variant = v;
   pl.tiles_m = (int)ceil_div(p.M, s.BM);
   pl.tiles_n = (int)ceil_div(p.N, s.BN);
-  const int kmax = s.thin == 1 ? kThinMKmax : kThinNKmax;
-  long long kps = ceil_div(ceil_div(p.K, std::max(1, split)), 8) * 8;
-  kps = std::min<long long>(std::max<long long>(kps, 8), kmax);
+  const int kmax = s.thin == 1 ? kThinMKmax : s.thin == 2 ? kThinNKmax : kThinTmaKmax;
+  const int kq = 8;  // K slice granule (the load batch / TMA chunk of the thin kernels)
+  long long kps = ceil_div(ceil_div(p.K, std::max(1, split)), kq) * kq;
+  kps = std::min<long long>(std::max<long long>(kps, kq), kmax);
   split = (int)ceil_div(p.K, kps);
   const long long tiles = (long long)pl.tiles_m * pl.tiles_n;
   const long long ctas = tiles * split;
@@ -164,7 +170,8 @@ inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool bet
   const double streamed = s.thin == 1 ? 4.0 * pl.tiles_m * (double)p.K * p.N
                                       : 4.0 * pl.tiles_n * (double)p.M * p.K;
   const double small = s.thin == 1 ? 4.0 * (double)p.M * p.K : 4.0 * (double)p.K * p.N;
-  const double part = split > 1 ? (double)ctas * s.BM * s.BN * 4.0 : 0.0;
+  const int groups = split;  // partial tiles per C tile
+  const double part = groups > 1 ? (double)tiles * groups * s.BM * s.BN * 4.0 : 0.0;
   const double mn_c = (double)p.M * p.N * 4.0 * (beta_nz ? 2.0 : 1.0);
   const double bytes = streamed + small + mn_c + 2.0 * part;
   pl.main_tiles = 0;
@@ -172,9 +179,13 @@ inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool bet
   pl.k_per_split = (int)kps;
   pl.group_m = 1;
   pl.ctas = (int)std::min<long long>(ctas, 0x7fffffffLL);
-  pl.launches = split > 1 ? 2 : 1;
-  pl.ws_bytes = split > 1 ? (size_t)part : 0;
-  pl.cycles = std::max(compute, bytes / 2800.0) + 2000.0 * pl.launches;
+  pl.launches = groups > 1 ? 2 : 1;
+  pl.ws_bytes = groups > 1 ? (size_t)part : 0;
+  // HBM is streamed at full speed only while every SM has work: scale the bandwidth by the
+  // average fraction of CTA slots the grid fills over its waves.
+  const long long waves = ceil_div(ctas, slots);
+  const double fill = (double)ctas / (double)(waves * slots);
+  pl.cycles = std::max(compute, bytes / (2800.0 * fill)) + 2000.0 * pl.launches;
   if (ctas > 0x7fffffffLL || pl.tiles_m > 65535 || pl.tiles_n > 65535 || split > 65535)
     pl.cycles = std::numeric_limits<double>::infinity();
   return pl;
@@ -393,9 +404,13 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
       continue;
     if (kVariants[v].kpair && (!p.kpair_ok || (force_v < 0 && !p.b_kmajor))) continue;
     const VariantShape &s = kVariants[v];
+    // 16-wide tiles exist for thin problems: the automatic plan keeps them for those
+    if (force_v < 0 && ((s.BM <= 16 && p.M > kThinMaxDim) || (s.BN <= 16 && p.N > kThinMaxDim)))
+      continue;
     if (s.thin) {
-      if (force_v < 0 && (s.thin == 1 ? p.M : p.N) > kThinMaxDim) continue;
-      const int kmax = s.thin == 1 ? kThinMKmax : kThinNKmax;
+      if (force_v < 0 && (s.thin != 2 ? p.M : p.N) > kThinMaxDim) continue;
+      if (s.thin == 3 && (!p.b_tma || p.transa)) continue;  // B read by TMA as stored
+      const int kmax = s.thin == 1 ? kThinMKmax : s.thin == 2 ? kThinNKmax : kThinTmaKmax;
       const int min_split = (int)ceil_div(p.K, kmax);
       if (force_split >= 1) {
         consider(model_thin(p, v, std::max(force_split, min_split), num_sms, beta_nz));

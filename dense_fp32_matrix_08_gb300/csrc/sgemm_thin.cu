@@ -5,6 +5,7 @@
 
 #include "sgemm_internal.h"
 #include "sgemm_thin.cuh"
+#include "sgemm_thin_tma.cuh"
 
 namespace sgemm {
 namespace {
@@ -31,9 +32,23 @@ cudaError_t thin_setup() {
     if (err == cudaSuccess) err = set_smem(thin::thin_m_kernel<false>, sm_m);
     if (err == cudaSuccess) err = set_smem(thin::thin_n_kernel<true>, sm_n);
     if (err == cudaSuccess) err = set_smem(thin::thin_n_kernel<false>, sm_n);
+    if (err == cudaSuccess)
+      err = set_smem(thin::thin_m_tma_kernel, thin::mt::smem_bytes(thin::mt::KMAX));
     g_err[dev] = err;
   });
   return g_err[dev];
+}
+
+cudaError_t launch_thin_m_tma(const thin::ThinParams &p, int *status, cudaStream_t stream) {
+  using namespace thin::mt;
+  if (p.k_per_split <= 0 || p.k_per_split > KMAX || p.k_per_split % KB != 0)
+    return cudaErrorInvalidValue;
+  CUtensorMap map_b;
+  if (!encode_map_2d(&map_b, p.B, p.K, p.N, p.ldb, BNC, KB, false)) return cudaErrorInvalidValue;
+  const dim3 grid(p.tiles_n, p.split, p.tiles_m);
+  thin::thin_m_tma_kernel<<<grid, THREADS, smem_bytes(p.k_per_split), stream>>>(map_b, p,
+                                                                                status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_thin(bool thin_m, const thin::ThinParams &p, bool vec, cudaStream_t stream) {

@@ -48,6 +48,56 @@ __device__ __forceinline__ float4 ld_stream4(const float *p) {
   return __ldcs(reinterpret_cast<const float4 *>(p));
 }
 
+// Copy the rows x cols block src (row stride ld, 0 outside rows_valid) into shared memory
+// transposed, dst[c * dpitch + r], with every thread of the block taking part. Loads are
+// issued 16 at a time before their stores, so the staging costs a few memory latencies
+// rather than one per element; consecutive threads read consecutive columns (coalesced).
+template <int THREADS>
+__device__ __forceinline__ void stage_transposed(const float *__restrict__ src, long long ld,
+                                                 int rows, int rows_valid, int cols,
+                                                 float *dst, int dpitch) {
+  constexpr int U = 16;
+  const int total = rows * cols;
+  for (int e0 = threadIdx.x; e0 < total; e0 += THREADS * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * THREADS;
+      const int r = e / cols, c = e - r * cols;
+      v[u] = (e < total && r < rows_valid) ? src[(long long)r * ld + c] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * THREADS;
+      const int r = e / cols, c = e - r * cols;
+      if (e < total) dst[c * dpitch + r] = v[u];
+    }
+  }
+}
+
+// The same without transposing: dst[r * dpitch + c] (columns beyond cols_valid are zero).
+template <int THREADS>
+__device__ __forceinline__ void stage_rows(const float *__restrict__ src, long long ld, int rows,
+                                           int cols, int cols_valid, float *dst, int dpitch) {
+  constexpr int U = 16;
+  const int total = rows * cols;
+  for (int e0 = threadIdx.x; e0 < total; e0 += THREADS * U) {
+    float v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * THREADS;
+      const int r = e / cols, c = e - r * cols;
+      v[u] = (e < total && c < cols_valid) ? src[(long long)r * ld + c] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int e = e0 + u * THREADS;
+      const int r = e / cols, c = e - r * cols;
+      if (e < total) dst[r * dpitch + c] = v[u];
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------
 // thin-M
 namespace m {
@@ -78,11 +128,8 @@ __global__ void __launch_bounds__(m::THREADS, 2) thin_m_kernel(const ThinParams 
   float *red = sm + (size_t)p.k_per_split * APITCH;
 
   // Stage A[m0 .. m0+MT) x [k0, k0+KS) as As[k][m] (rows beyond M are zero).
-  for (int e = threadIdx.x; e < MT * KS; e += THREADS) {
-    const int mm = e / KS, k = e - mm * KS;
-    const int gm = m0 + mm;
-    As[k * APITCH + mm] = gm < p.M ? p.A[(long long)gm * p.lda + (k0 + k)] : 0.0f;
-  }
+  stage_transposed<THREADS>(p.A + (long long)m0 * p.lda + k0, p.lda, MT, min(MT, p.M - m0),
+                            KS, As, APITCH);
   __syncthreads();
 
   const int g = threadIdx.x / TPG, j = threadIdx.x % TPG;
@@ -224,10 +271,7 @@ __global__ void __launch_bounds__(n::THREADS, 1) thin_n_kernel(const ThinParams 
   float *Bs = sm;
 
   // Stage B[k0 .. k0+KS) x [c0, c0+NC) as Bs[k][c] (columns beyond N are zero).
-  for (int e = threadIdx.x; e < KS * NC; e += THREADS) {
-    const int k = e / NC, c = e - k * NC;
-    Bs[e] = c0 + c < p.N ? p.B[(long long)(k0 + k) * p.ldb + (c0 + c)] : 0.0f;
-  }
+  stage_rows<THREADS>(p.B + (long long)k0 * p.ldb + c0, p.ldb, KS, NC, min(NC, p.N - c0), Bs, NC);
   __syncthreads();
 
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

@@ -15,10 +15,11 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 41  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 42  # compiled tile configurations; checked against the library below
 TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
+THIN_M_TMA = 41  # TMA-fed thin-M: B must be TMA-addressable
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -108,9 +109,11 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
+    if not aligned and variant == THIN_M_TMA:
+        pytest.skip("the TMA-fed thin-M kernel reads B by TMA: aligned B only")
     for (M, N, K) in RAGGED:
         A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
-        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS:
+        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS + (THIN_M_TMA,):
             # TMA needs ld % 4 == 0: pad the rows
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
         elif variant in KPAIR_VARIANTS:  # aligned A; B and C with odd ld and offsets
@@ -158,15 +161,19 @@ THIN_N_SHAPES = [(1, 1, 1), (255, 5, 7), (1024, 16, 2049), (1000, 16, 4100), (41
                  (3000, 16, 1100)]
 
 
-@pytest.mark.parametrize("kind", ["m", "n"])
-@pytest.mark.parametrize("split", [0, 1, 5])
+@pytest.mark.parametrize("kind", ["m", "n", "mt"])
+@pytest.mark.parametrize("split", [0, 1, 5, 17])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_thin_kernels(kind, split, aligned):
     """The thin-M / thin-N streaming kernels, forced, on ragged and slice-boundary shapes:
     K slices that are not a multiple of the 8-deep load batch, column quads and rows that
-    cross N and M, one slice (alpha / beta in the kernel) and several (reduce kernel)."""
-    variant = THIN_M if kind == "m" else THIN_N
-    for (M, N, K) in (THIN_M_SHAPES if kind == "m" else THIN_N_SHAPES):
+    cross N and M, one slice (alpha / beta in the kernel) and several (reduce kernel).
+    The TMA-fed thin-M kernel ("mt") needs an aligned B; split 17 on K = 2049 / 1100 gives
+    slices that end inside a 32-row B tile."""
+    if kind == "mt" and not aligned:
+        pytest.skip("the TMA-fed thin-M kernel reads B by TMA: aligned B only")
+    variant = {"m": THIN_M, "n": THIN_N, "mt": THIN_M_TMA}[kind]
+    for (M, N, K) in (THIN_N_SHAPES if kind == "n" else THIN_M_SHAPES):
         A, B, C = make_inputs(M, N, K, seed=M + 3 * N + 5 * K + split)
         if aligned:
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
