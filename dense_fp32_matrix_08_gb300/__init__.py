@@ -22,7 +22,7 @@ __all__ = [
     "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_status", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
     "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
-    "sgemm_f32_tune_load", "sgemm", "EXPORTED",
+    "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -33,7 +33,8 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_3xtf32",
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status",
             "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
-            "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load")
+            "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load",
+            "sgemm_f32_host")
 
 
 class SgemmError(RuntimeError):
@@ -65,6 +66,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_tune_clear.argtypes = []
     L.sgemm_f32_tune_save.argtypes = [ctypes.c_char_p]
     L.sgemm_f32_tune_load.argtypes = [ctypes.c_char_p]
+    L.sgemm_f32_host.argtypes = gemm + [vp]
     L.sgemv_f32.argtypes = [i, i, i, f, vp, i, vp, i, f, vp, i, vp]
     L.sdot_f32.argtypes = [i, vp, i, vp, i, vp, vp]
     L.sgemm_f32_colmajor.argtypes = [i, i] + gemm + [vp]
@@ -147,6 +149,29 @@ def sgemm_f32_autotune(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, 
                                 _ptr(B), ldb, beta, _ptr(C), ldc, int(reps), _stream(stream),
                                 ctypes.byref(v), ctypes.byref(sp), ctypes.byref(ms))
     return {"status": rc, "variant": v.value, "split": sp.value, "ms": ms.value}
+
+
+def _host_ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    import torch
+    if isinstance(x, torch.Tensor):
+        if x.dtype != torch.float32:
+            raise TypeError("tensor operands must be float32")
+        if x.is_cuda:
+            raise TypeError("sgemm_f32_host takes host (CPU) tensors")
+        return x.data_ptr() or None
+    raise TypeError(f"cannot pass {type(x).__name__} as a host pointer")
+
+
+def sgemm_f32_host(M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None) -> int:
+    """C = alpha A B + beta C with A, B, C in host memory (pinned for overlap); the GPU
+    computes it in row blocks while the copies of neighbouring blocks run. Asynchronous on
+    `stream`: synchronise it before reading C."""
+    return lib.sgemm_f32_host(M, N, K, alpha, _host_ptr(A), lda, _host_ptr(B), ldb, beta,
+                              _host_ptr(C), ldc, _stream(stream))
 
 
 def sgemm_f32_tune_count() -> int:

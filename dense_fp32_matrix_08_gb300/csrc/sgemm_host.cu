@@ -1,0 +1,171 @@
+// sgemm_f32_host: C = alpha * A * B + beta * C with A, B and C in host memory. The product
+// runs on the GPU in row blocks; the host <-> device copies of one block overlap the
+// computation of its neighbours:
+//
+//   copy-in stream   B   A0 C0   A1 C1   .......  A2 C2 (after D2H 0) ...
+//   compute stream             GEMM 0    GEMM 1    GEMM 2 ...
+//   copy-out stream                      C0 out    C1 out   ...
+//
+// Device buffers (B whole; A and C blocks, double-buffered) come from the library's
+// workspace pool on the caller's stream and go back to it when the work is done.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <mutex>
+#include <vector>
+
+#include "../../include/sgemm_f32.h"
+#include "sgemm_internal.h"
+#include "sgemm_plan.h"
+
+namespace sgemm {
+namespace {
+
+struct CopyStreams {
+  std::once_flag once;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+CopyStreams g_copy[64];
+
+cudaError_t copy_streams(cudaStream_t *in, cudaStream_t *out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  CopyStreams &c = g_copy[dev];
+  std::call_once(c.once, [&c]() {
+    c.err = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
+    if (c.err == cudaSuccess) c.err = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
+  });
+  *in = c.in;
+  *out = c.out;
+  return c.err;
+}
+
+// Events of one call; destroyed after enqueueing (CUDA releases them once complete).
+struct Events {
+  std::vector<cudaEvent_t> ev;
+  ~Events() {
+    for (cudaEvent_t e : ev) cudaEventDestroy(e);
+  }
+  cudaError_t make(cudaEvent_t *out) {
+    cudaError_t e = cudaEventCreateWithFlags(out, cudaEventDisableTiming);
+    if (e == cudaSuccess) ev.push_back(*out);
+    return e;
+  }
+};
+
+}  // namespace
+}  // namespace sgemm
+
+using namespace sgemm;
+
+extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, int lda,
+                              const float *B, int ldb, float beta, float *C, int ldc,
+                              cudaStream_t stream) {
+  Problem pr{M, N, K, lda, ldb, ldc};
+  int rc = validate(pr, alpha, A != nullptr, B != nullptr, C != nullptr);
+  if (rc != 0) return rc;
+  if (M == 0 || N == 0) return 0;
+  const bool reads_ab = K > 0 && alpha != 0.0f;
+  if (!reads_ab && beta == 1.0f) return 0;  // C unchanged
+  int num_sms = 0;
+  cudaError_t e = device_setup(&num_sms);
+  if (e != cudaSuccess) return (int)e;
+  cudaStream_t s_in = nullptr, s_out = nullptr;
+  e = copy_streams(&s_in, &s_out);
+  if (e != cudaSuccess) return (int)e;
+
+  // Row blocks: about 2048 rows (enough tiles for several waves of the GEMM kernel),
+  // at most 8 blocks, a multiple of 128 rows.
+  const int nb = std::max(1, std::min(8, M / 2048));
+  const int mb = (int)std::min<long long>(M, ceil_div(ceil_div(M, nb), 128) * 128);
+  const int blocks = (int)ceil_div(M, mb);
+  const bool need_c_in = beta != 0.0f;
+
+  const size_t b_bytes = reads_ab ? (size_t)K * N * 4 : 0;
+  const size_t a_bytes = reads_ab ? (size_t)mb * K * 4 : 0;
+  const size_t c_bytes = (size_t)mb * N * 4;
+  float *dB = nullptr, *dA[2] = {nullptr, nullptr}, *dC[2] = {nullptr, nullptr};
+  cudaMemPool_t pool = workspace_pool();
+  auto alloc = [&](float **p, size_t bytes) {
+    if (bytes == 0 || e != cudaSuccess) return;
+    e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(p), bytes, pool, stream);
+  };
+  alloc(&dB, b_bytes);
+  for (int q = 0; q < std::min(2, blocks); ++q) {
+    alloc(&dA[q], a_bytes);
+    alloc(&dC[q], c_bytes);
+  }
+  Events evs;
+  cudaEvent_t ev_start = nullptr;
+  if (e == cudaSuccess) e = evs.make(&ev_start);
+  if (e == cudaSuccess) e = cudaEventRecord(ev_start, stream);  // buffers are allocated
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_in, ev_start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_start, 0);
+
+  auto rows_of = [&](int i) { return std::min(mb, M - i * mb); };
+  std::vector<cudaEvent_t> ev_in(blocks, nullptr), ev_done(blocks, nullptr),
+      ev_out(blocks, nullptr);
+  auto copy_in = [&](int i) {  // on s_in: A and C rows of block i into buffer i % 2
+    const int r0 = i * mb, rows = rows_of(i);
+    if (e == cudaSuccess && reads_ab)
+      e = cudaMemcpy2DAsync(dA[i % 2], (size_t)K * 4, A + (long long)r0 * lda, (size_t)lda * 4,
+                            (size_t)K * 4, rows, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess && need_c_in)
+      e = cudaMemcpy2DAsync(dC[i % 2], (size_t)N * 4, C + (long long)r0 * ldc, (size_t)ldc * 4,
+                            (size_t)N * 4, rows, cudaMemcpyHostToDevice, s_in);
+    if (e == cudaSuccess) e = evs.make(&ev_in[i]);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_in[i], s_in);
+  };
+
+  if (e == cudaSuccess && reads_ab)
+    e = cudaMemcpy2DAsync(dB, (size_t)N * 4, B, (size_t)ldb * 4, (size_t)N * 4, K,
+                          cudaMemcpyHostToDevice, s_in);
+  copy_in(0);
+  if (blocks > 1) copy_in(1);
+  for (int i = 0; i < blocks && e == cudaSuccess; ++i) {
+    const int r0 = i * mb, rows = rows_of(i);
+    e = cudaStreamWaitEvent(stream, ev_in[i], 0);
+    if (e != cudaSuccess) break;
+    // the block's product on the caller's stream, through the library's own entry point
+    rc = sgemm_f32(rows, N, K, alpha, reads_ab ? dA[i % 2] : nullptr, std::max(1, K),
+                   reads_ab ? dB : nullptr, N, beta, dC[i % 2], N, stream);
+    if (rc != 0) break;
+    e = evs.make(&ev_done[i]);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_done[i], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_done[i], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpy2DAsync(C + (long long)r0 * ldc, (size_t)ldc * 4, dC[i % 2], (size_t)N * 4,
+                            (size_t)N * 4, rows, cudaMemcpyDeviceToHost, s_out);
+    if (e == cudaSuccess) e = evs.make(&ev_out[i]);
+    if (e == cudaSuccess) e = cudaEventRecord(ev_out[i], s_out);
+    // block i + 2 reuses buffer i % 2 once block i's result has left it
+    if (e == cudaSuccess && i + 2 < blocks) {
+      e = cudaStreamWaitEvent(s_in, ev_out[i], 0);
+      copy_in(i + 2);
+    }
+  }
+  // The caller's stream owns the result: it waits for the last copies out, then frees.
+  for (int i = 0; i < blocks; ++i)
+    if (ev_out[i] != nullptr) {
+      const cudaError_t w = cudaStreamWaitEvent(stream, ev_out[i], 0);
+      if (e == cudaSuccess) e = w;
+    }
+  if (ev_start != nullptr && (e != cudaSuccess || rc != 0)) {
+    // on an error the copy streams may still reference the buffers: join them first
+    cudaEvent_t j1 = nullptr, j2 = nullptr;
+    if (evs.make(&j1) == cudaSuccess && cudaEventRecord(j1, s_in) == cudaSuccess)
+      cudaStreamWaitEvent(stream, j1, 0);
+    if (evs.make(&j2) == cudaSuccess && cudaEventRecord(j2, s_out) == cudaSuccess)
+      cudaStreamWaitEvent(stream, j2, 0);
+  }
+  for (float *p : {dB, dA[0], dA[1], dC[0], dC[1]})
+    if (p != nullptr) {
+      const cudaError_t f = cudaFreeAsync(p, stream);
+      if (e == cudaSuccess) e = f;
+    }
+  if (rc != 0) return rc;
+  return (int)e;
+}

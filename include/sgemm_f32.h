@@ -264,6 +264,19 @@ int sgemm_f32_3xtf32_status(int *status);
  * stopped computing and the result of that call is not valid. */
 int sgemm_f32_status(int *status);
 
+/* C = alpha * A * B + beta * C with A, B and C in HOST memory (row-major, the ld rules of
+ * sgemm_f32). The product runs on the GPU in row blocks of about 2048 rows: B is copied to
+ * the device once, and the copies of a block's A and C rows in and of its C rows out run on
+ * two library-owned copy streams that overlap the GEMMs of the neighbouring blocks, which
+ * run on `stream`. Device buffers come from the library's workspace pool (B, and two
+ * A-block and C-block buffers) and are released in stream order.
+ * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
+ * overlap; pageable memory works, with copies that do not overlap.
+ * Asynchronous on `stream`: C on the host is final once `stream` has been synchronised;
+ * A, B and C must stay valid until then. Returns the sgemm_f32 codes. */
+int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, int lda, const float *B,
+                   int ldb, float beta, float *C, int ldc, cudaStream_t stream);
+
 /* ---- Measured plan selection ("GPU GEMM 优化完全拆解（二）", autotuning section: sweep the
  * legal tile parameters and keep the fastest set, which differs from GPU to GPU). ----
  *
