@@ -83,6 +83,17 @@ def kernel_source_hash() -> str:
     return h.hexdigest()
 
 
+def git_sha():
+    """The checked-out commit, or None where the tree is a copy without .git."""
+    import subprocess
+    try:
+        out = subprocess.run(["git", "rev-parse", "HEAD"], cwd=ROOT, capture_output=True,
+                             text=True, timeout=10)
+        return out.stdout.strip() or None if out.returncode == 0 else None
+    except (OSError, subprocess.SubprocessError):
+        return None
+
+
 def recorded_traffic(workload: str, plan: dict):
     """DRAM bytes per launch of the GEMM kernel from the committed ncu capture, or None if
     it was taken on another workload, plan or kernel source."""
@@ -487,6 +498,7 @@ def our_arm(args, dist: Dist):
             "gpu_launches": plan["launches"] * args.steps,
             "plan": {k: plan[k] for k in ("variant", "split", "main_tiles", "launches",
                                           "ws_bytes")},
+            "source_sha256": kernel_source_hash(), "git_sha": git_sha(),
             "impl": "ours",
         }
         if secondary:

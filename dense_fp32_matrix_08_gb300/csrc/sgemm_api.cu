@@ -6,6 +6,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
 #include <cstdlib>
 #include <limits>
 #include <mutex>
@@ -136,6 +137,40 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
   e = Entry{pr.M, pr.N, pr.K, num_sms, force_v, force_split, flags, true,
             make_plan(pr, alpha, beta, num_sms, force_v, force_split)};
   return e.plan;
+}
+
+// SGEMM_F32_FORCE="v" or "v:s" (environment, read once per process) pins the automatic
+// plan to configuration v with split argument s, as sgemm_f32_forced would: a benchmarking
+// switch. Problems the configuration cannot run keep their automatic plan.
+static bool env_force(int *v, int *s) {
+  static int ev = -1, es = 0;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    const char *t = std::getenv("SGEMM_F32_FORCE");
+    int a = -1, b = 0;
+    if (t != nullptr && std::sscanf(t, "%d:%d", &a, &b) >= 1 && a >= 0 && a < kNumVariants &&
+        b >= -64 && b <= 64) {
+      ev = a;
+      es = b;
+    }
+  });
+  if (ev < 0) return false;
+  *v = ev;
+  *s = es;
+  return true;
+}
+
+// The automatic plan: SGEMM_F32_FORCE if set and applicable, else a plan recorded by
+// sgemm_f32_autotune, else the cost model.
+static Plan automatic_plan(const Problem &pr, float alpha, float beta, int num_sms) {
+  int v = -1, sp = 0;
+  if (env_force(&v, &sp)) {
+    const Plan pl = cached_plan(pr, alpha, beta, num_sms, v, sp);
+    if (pl.variant >= 0 || alpha == 0.0f || pr.K == 0) return pl;
+  }
+  if (tuned_lookup(pr, beta != 0.0f, num_sms, &v, &sp))
+    return cached_plan(pr, alpha, beta, num_sms, v, sp);
+  return cached_plan(pr, alpha, beta, num_sms, -1, 0);
 }
 
 static int *status_word() {
@@ -351,14 +386,9 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
-  if (force_v < 0 && force_split == 0) {  // a plan measured by sgemm_f32_autotune wins
-    int tv = -1, ts = 0;
-    if (tuned_lookup(pr, beta != 0.0f, num_sms, &tv, &ts)) {
-      force_v = tv;
-      force_split = ts;
-    }
-  }
-  Plan pl = cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
+  Plan pl = (force_v < 0 && force_split == 0)
+                ? automatic_plan(pr, alpha, beta, num_sms)
+                : cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
   // No candidate fitted (a forced configuration whose workspace exceeds the limits).
   if (pl.variant < 0 && alpha != 0.0f && K > 0) return force_v >= 0 ? kErrBadVariant
                                                                     : kErrWorkspace;
@@ -469,11 +499,7 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
   if (M == 0 || N == 0) {
     pl.variant = -1;
   } else {
-    int tv = -1, ts = 0;
-    if (tuned_lookup(pr, beta != 0.0f, num_sms, &tv, &ts))
-      pl = cached_plan(pr, alpha, beta, num_sms, tv, ts);
-    else
-      pl = cached_plan(pr, alpha, beta, num_sms, -1, 0);
+    pl = automatic_plan(pr, alpha, beta, num_sms);
   }
   if (variant) *variant = pl.variant;
   if (split) *split = pl.split;

@@ -177,6 +177,12 @@ int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);
 
+/* Benchmarking switch: when the environment variable SGEMM_F32_FORCE is "v" or "v:s" at the
+ * first call in the process, every automatic plan (sgemm_f32, sgemm_f32_ex, sgemm_f32_ws,
+ * sgemm_f32_noalloc, sgemm_f32_host, sgemm_f32_plan) is the one sgemm_f32_forced would make
+ * with variant v and split s, for the problems that configuration can run; the others keep
+ * their automatic plan. It takes precedence over plans recorded by sgemm_f32_autotune. */
+
 /* sgemm_f32_ex with the plan forced (variant and split as in sgemm_f32_forced). Returns
  * -14 also when the forced configuration has no path for these transpose flags or this
  * alignment:

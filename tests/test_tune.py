@@ -73,3 +73,27 @@ def test_bad_lines_and_paths(tmp_path):
     assert sg.lib.sgemm_f32_tune_load(None) == -1
     assert sg.lib.sgemm_f32_tune_save(None) == -1
     assert sg.sgemm_f32_tune_save(os.path.join(tmp_path, "no", "such", "dir.txt")) == -2
+
+
+def test_env_force_switch():
+    """SGEMM_F32_FORCE pins the automatic plan of every entry point to a configuration (a
+    benchmarking switch), except where that configuration cannot run the problem."""
+    import subprocess
+    import sys
+    code = ("import dense_fp32_matrix_08_gb300 as sg\n"
+            "p = sg.sgemm_f32_plan(4096, 4096, 4096, 4096, 4096, 4096, 1.0, 1.0, 152)\n"
+            "q = sg.sgemm_f32_plan(64, 64, 64, 64, 64, 64, 1.0, 1.0, 152)\n"
+            "print(p['variant'], p['split'], q['variant'])\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, SGEMM_F32_FORCE="16:1")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                         text=True, check=True).stdout.split()
+    assert out[:2] == ["16", "1"] and out[2] == "16"
+    # an out-of-range configuration is ignored: the automatic plans stay as they are
+    env = dict(os.environ, SGEMM_F32_FORCE="999")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, env=env, capture_output=True,
+                         text=True, check=True).stdout.split()
+    plain = subprocess.run([sys.executable, "-c", code], cwd=root,
+                           env={k: v for k, v in os.environ.items() if k != "SGEMM_F32_FORCE"},
+                           capture_output=True, text=True, check=True).stdout.split()
+    assert out == plain
