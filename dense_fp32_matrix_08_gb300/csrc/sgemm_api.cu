@@ -40,10 +40,11 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},
     VariantKernels{},  // more k-major TMA-fed instances (sgemm_tma.cu)
     VariantKernels{},
-    VariantKernels{},  // TMA-fed thin-M with cluster reduction (sgemm_thin.cu)
+    VariantKernels{},  // TMA-fed thin-M and thin-N kernels (sgemm_thin.cu)
+    VariantKernels{},
 };
 static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
-                  kThinNVariant == 34 && kThinTmaVariant == 41 && kNumVariants == 42,
+                  kThinNVariant == 34 && kThinTmaVariant == 41 && kNumVariants == 43,
               "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
@@ -239,8 +240,8 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     tp.vec_c = vec_c ? 1 : 0;
     cudaError_t te;
     int parts = pl.split;  // partial tiles per C tile for the reduce kernel
-    if (vs.thin == 3) {
-      te = launch_thin_m_tma(tp, status_word(), stream);
+    if (vs.thin >= 3) {
+      te = launch_thin_tma(vs.thin == 4, tp, status_word(), stream);
     } else {
       // 128-bit loads of the streamed operand: B rows (thin-M) or A rows (thin-N)
       const bool vec = vs.thin == 1 ? (pr.ldb % 4 == 0 && aligned16(B))

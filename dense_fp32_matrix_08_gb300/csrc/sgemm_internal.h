@@ -19,6 +19,10 @@ cudaMemPool_t workspace_pool();
 // box read as zero. Returns false if the driver rejects the description.
 bool encode_map_2d(CUtensorMap *map, const float *ptr, long long rows, long long cols,
                    long long ld, int box_cols, int box_rows, bool swizzle128);
+// The same with a chosen swizzle span: 0 (none), 32, 64 or 128 bytes (box_cols * 4 must
+// equal the span when it is not 0).
+bool encode_map_2d_swizzle(CUtensorMap *map, const float *ptr, long long rows, long long cols,
+                           long long ld, int box_cols, int box_rows, int swizzle_bytes);
 
 struct GemmParams;
 struct Problem;
@@ -35,9 +39,10 @@ struct ThinParams;
 // of the streamed operand allowed).
 cudaError_t thin_setup();
 cudaError_t launch_thin(bool thin_m, const thin::ThinParams &p, bool vec, cudaStream_t stream);
-// TMA-fed thin-M kernel (sgemm_thin_tma.cuh): p.split CTAs along K, p.k_per_split a
-// multiple of 8 and at most 1024; B TMA-addressable.
-cudaError_t launch_thin_m_tma(const thin::ThinParams &p, int *status, cudaStream_t stream);
+// TMA-fed thin kernel (sgemm_thin_tma.cuh): thin-M (B TMA-addressable) or thin-N (A
+// TMA-addressable); p.split CTAs along K, p.k_per_split a multiple of 8, at most 1024.
+cudaError_t launch_thin_tma(bool thin_n, const thin::ThinParams &p, int *status,
+                            cudaStream_t stream);
 
 // TMA-fed GEMM (sgemm_ffma_tma.cuh): one-time kernel attributes for the current device, and
 // a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb); for

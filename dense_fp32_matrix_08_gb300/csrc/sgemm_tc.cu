@@ -380,15 +380,26 @@ static EncodeTiledFn encode_fn() {
 
 bool encode_map_2d(CUtensorMap *map, const float *ptr, long long rows, long long cols,
                    long long ld, int box_cols, int box_rows, bool swizzle128) {
+  return encode_map_2d_swizzle(map, ptr, rows, cols, ld, box_cols, box_rows,
+                               swizzle128 ? 128 : 0);
+}
+
+bool encode_map_2d_swizzle(CUtensorMap *map, const float *ptr, long long rows, long long cols,
+                           long long ld, int box_cols, int box_rows, int swizzle_bytes) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle_bytes == 32) swz = CU_TENSOR_MAP_SWIZZLE_32B;
+  else if (swizzle_bytes == 64) swz = CU_TENSOR_MAP_SWIZZLE_64B;
+  else if (swizzle_bytes == 128) swz = CU_TENSOR_MAP_SWIZZLE_128B;
+  else if (swizzle_bytes != 0) return false;
   const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   const cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
   const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(ptr), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+             swz,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

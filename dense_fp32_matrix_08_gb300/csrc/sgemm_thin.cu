@@ -33,21 +33,32 @@ cudaError_t thin_setup() {
     if (err == cudaSuccess) err = set_smem(thin::thin_n_kernel<true>, sm_n);
     if (err == cudaSuccess) err = set_smem(thin::thin_n_kernel<false>, sm_n);
     if (err == cudaSuccess)
-      err = set_smem(thin::thin_m_tma_kernel, thin::mt::smem_bytes(thin::mt::KMAX));
+      err = set_smem(thin::thin_tma_kernel<false>, thin::mt::smem_bytes(thin::mt::KMAX));
+    if (err == cudaSuccess)
+      err = set_smem(thin::thin_tma_kernel<true>, thin::mt::smem_bytes(thin::mt::KMAX));
     g_err[dev] = err;
   });
   return g_err[dev];
 }
 
-cudaError_t launch_thin_m_tma(const thin::ThinParams &p, int *status, cudaStream_t stream) {
+cudaError_t launch_thin_tma(bool thin_n, const thin::ThinParams &p, int *status,
+                            cudaStream_t stream) {
   using namespace thin::mt;
   if (p.k_per_split <= 0 || p.k_per_split > KMAX || p.k_per_split % KB != 0)
     return cudaErrorInvalidValue;
-  CUtensorMap map_b;
-  if (!encode_map_2d(&map_b, p.B, p.K, p.N, p.ldb, BNC, KB, false)) return cudaErrorInvalidValue;
-  const dim3 grid(p.tiles_n, p.split, p.tiles_m);
-  thin::thin_m_tma_kernel<<<grid, THREADS, smem_bytes(p.k_per_split), stream>>>(map_b, p,
-                                                                                status);
+  CUtensorMap map_s;
+  const size_t smem = smem_bytes(p.k_per_split);
+  if (thin_n) {  // A streams as [256 m][8 k] tiles, 32-byte swizzle
+    if (!encode_map_2d_swizzle(&map_s, p.A, p.M, p.K, p.lda, KC, BNC, 32))
+      return cudaErrorInvalidValue;
+    const dim3 grid(p.tiles_m, p.split, p.tiles_n);
+    thin::thin_tma_kernel<true><<<grid, THREADS, smem, stream>>>(map_s, p, status);
+  } else {  // B streams as [8 k][256 n] tiles
+    if (!encode_map_2d(&map_s, p.B, p.K, p.N, p.ldb, BNC, KC, false))
+      return cudaErrorInvalidValue;
+    const dim3 grid(p.tiles_n, p.split, p.tiles_m);
+    thin::thin_tma_kernel<false><<<grid, THREADS, smem, stream>>>(map_s, p, status);
+  }
   return cudaGetLastError();
 }
 

@@ -15,11 +15,12 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 42  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 43  # compiled tile configurations; checked against the library below
 TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
 THIN_M_TMA = 41  # TMA-fed thin-M: B must be TMA-addressable
+THIN_N_TMA = 42  # TMA-fed thin-N: A must be TMA-addressable
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -109,11 +110,11 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
-    if not aligned and variant == THIN_M_TMA:
-        pytest.skip("the TMA-fed thin-M kernel reads B by TMA: aligned B only")
+    if not aligned and variant in (THIN_M_TMA, THIN_N_TMA):
+        pytest.skip("the TMA-fed thin kernels read the streamed operand by TMA: aligned only")
     for (M, N, K) in RAGGED:
         A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
-        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS + (THIN_M_TMA,):
+        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS + (THIN_M_TMA, THIN_N_TMA):
             # TMA needs ld % 4 == 0: pad the rows
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
         elif variant in KPAIR_VARIANTS:  # aligned A; B and C with odd ld and offsets
@@ -161,7 +162,7 @@ THIN_N_SHAPES = [(1, 1, 1), (255, 5, 7), (1024, 16, 2049), (1000, 16, 4100), (41
                  (3000, 16, 1100)]
 
 
-@pytest.mark.parametrize("kind", ["m", "n", "mt"])
+@pytest.mark.parametrize("kind", ["m", "n", "mt", "nt"])
 @pytest.mark.parametrize("split", [0, 1, 5, 17])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_thin_kernels(kind, split, aligned):
@@ -170,10 +171,10 @@ def test_thin_kernels(kind, split, aligned):
     cross N and M, one slice (alpha / beta in the kernel) and several (reduce kernel).
     The TMA-fed thin-M kernel ("mt") needs an aligned B; split 17 on K = 2049 / 1100 gives
     slices that end inside a 32-row B tile."""
-    if kind == "mt" and not aligned:
-        pytest.skip("the TMA-fed thin-M kernel reads B by TMA: aligned B only")
-    variant = {"m": THIN_M, "n": THIN_N, "mt": THIN_M_TMA}[kind]
-    for (M, N, K) in (THIN_N_SHAPES if kind == "n" else THIN_M_SHAPES):
+    if kind in ("mt", "nt") and not aligned:
+        pytest.skip("the TMA-fed thin kernels read the streamed operand by TMA: aligned only")
+    variant = {"m": THIN_M, "n": THIN_N, "mt": THIN_M_TMA, "nt": THIN_N_TMA}[kind]
+    for (M, N, K) in (THIN_N_SHAPES if kind in ("n", "nt") else THIN_M_SHAPES):
         A, B, C = make_inputs(M, N, K, seed=M + 3 * N + 5 * K + split)
         if aligned:
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
