@@ -12,11 +12,18 @@
 // Data flow (three launches on the caller's stream):
 //  1. split_rows_kernel:  A (M x K, lda) -> A_hi, A_lo (Mp x Kp, K-major, zero padded)
 //  2. split_cols_kernel:  B (K x N, ldb) -> B_hi, B_lo (Np x Kp, K-major = B transposed)
-//  3. tc3_kernel:         one CTA per 128 x 128 tile of C. Warp 0 lane 0 streams the four
-//     operand tiles of each 32-wide K block into a 3-stage shared-memory ring with TMA
-//     (128-byte swizzle); warp 1 lane 0 issues 12 tcgen05.mma (kind::tf32, M=128 N=128
-//     K=8) per K block into one TMEM accumulator (128 lanes x 128 FP32 columns); all four
-//     warps then read the accumulator with tcgen05.ld and apply alpha / beta.
+//  3. tc3_kernel:         persistent (one CTA per SM, 128 x 128 C tiles in grouped order,
+//     tile t, t + grid, ...), warp-specialised:
+//       warp 0 lane 0   streams the four operand tiles of each 32-wide K block (A_hi, A_lo,
+//                       B_hi, B_lo, 128 x 32 each) into a 3-stage shared-memory ring with
+//                       TMA (128-byte swizzle);
+//       warp 1 lane 0   issues 12 tcgen05.mma (kind::tf32, M=128 N=128 K=8) per K block
+//                       into one of two TMEM accumulators (128 lanes x 128 FP32 columns
+//                       each), alternating per tile;
+//       warps 2 - 5     drain the other accumulator meanwhile: tcgen05.ld, a per-warp
+//                       transpose in shared memory, and coalesced alpha / beta row stores.
+//     The epilogue of tile i thus overlaps the MMAs of tile i + 1. (A 128 x 256 tile, all
+//     512 TMEM columns, measured the same at 8192^3 and slower at 4096^3: fewer tiles.)
 // Every wait on an mbarrier is bounded: a wait that gives up records an error in a device
 // status word (read with sgemm_f32_3xtf32_status) and the CTA still frees its TMEM.
 #include <cuda.h>
@@ -34,14 +41,20 @@
 namespace sgemm {
 namespace tc {
 
-constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3, THREADS = 128;
-constexpr int TILE_BYTES = BM * BK * 4;      // one 128 x 32 FP32 operand tile (BN == BM)
-constexpr int STAGE_BYTES = 4 * TILE_BYTES;  // A_hi, A_lo, B_hi, B_lo
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;  // + alignment slack, barriers
-constexpr uint32_t TMEM_COLS = 128;
+constexpr int BM = 128, BN = 128, BK = 32, STAGES = 3;
+constexpr int EPI_WARPS = 4, THREADS = 32 * (2 + EPI_WARPS);  // producer, MMA, epilogue
+constexpr int A_TILE = BM * BK * 4;          // one 128 x 32 FP32 operand tile of A
+constexpr int B_TILE = BN * BK * 4;          // one 256 x 32 FP32 operand tile of B^T
+constexpr int STAGE_BYTES = 2 * A_TILE + 2 * B_TILE;  // A_hi, A_lo, B_hi, B_lo
+constexpr int EPI_PITCH = 33;                // transpose buffer row pitch (floats)
+constexpr int EPI_BYTES = EPI_WARPS * 32 * EPI_PITCH * 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + EPI_BYTES + 128;
+constexpr uint32_t ACC_COLS = BN;            // one accumulator: BN FP32 columns
+constexpr uint32_t TMEM_COLS = 2 * ACC_COLS;
 
-static_assert(BM == BN, "operand tiles share one size");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA on sm_103a");
+static_assert(TMEM_COLS <= 512, "two accumulators fit in TMEM");
+static_assert(BN % 16 == 0 && BN <= 256, "tcgen05.mma N for M = 128");
 
 // Instruction descriptor of tcgen05.mma kind::tf32: D in FP32 (bits 4-5 = 1), A and B in
 // TF32 (bits 7-9 and 10-12 = 2), both K-major (bits 15, 16 = 0), N / 8 in bits 17-22,
@@ -84,7 +97,7 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
-// D[tmem] (+)= A[smem desc] * B[smem desc]^T, 128 x 128 x 8, TF32 inputs, FP32 accumulation.
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, 128 x BN x 8, TF32 inputs, FP32 accumulation.
 __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                          uint32_t accumulate) {
   asm volatile(
@@ -204,22 +217,29 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = saddr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;  // swizzle atoms need 1024-byte alignment
-  const uint32_t bars = base + STAGES * STAGE_BYTES;
-  // barriers: full[s] at bars + 8 s, empty[s] at bars + 8 (STAGES + s), accum after them
-  const uint32_t accum_bar = bars + 8 * (2 * STAGES);
-  const uint32_t tmem_slot = accum_bar + 8;
+  float *epi = reinterpret_cast<float *>(smem_raw + (base - raw) + STAGES * STAGE_BYTES);
+  const uint32_t bars = base + STAGES * STAGE_BYTES + EPI_BYTES;
+  // full[s] at bars + 8 s, empty[s] at bars + 8 (STAGES + s), acc_full[b] and acc_empty[b]
+  // after them, then the TMEM address slot
+  const uint32_t acc_full = bars + 8 * (2 * STAGES);
+  const uint32_t acc_empty = acc_full + 16;
+  const uint32_t tmem_slot = acc_empty + 16;
   volatile uint32_t *tmem_slot_ptr =
       reinterpret_cast<volatile uint32_t *>(smem_raw + (tmem_slot - raw));
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int tiles = p.tiles_m * p.tiles_n;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bars + 8 * s, 1);
       mbar_init(bars + 8 * (STAGES + s), 1);
     }
-    mbar_init(accum_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full + 8 * b, 1);
+      mbar_init(acc_empty + 8 * b, EPI_WARPS);
+    }
     mbar_init_fence();
   }
   if (warp == 0) {
@@ -231,89 +251,120 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot_ptr;
 
-  int tm, tn;
-  tile_coords(blockIdx.x, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-
   if (warp == 0 && lane == 0) {
-    // ---- TMA producer
+    // ---- TMA producer: every K block of every tile of this CTA, in order
     tma_prefetch_map(&map_ah);
     tma_prefetch_map(&map_al);
     tma_prefetch_map(&map_bh);
     tma_prefetch_map(&map_bl);
-    int issued = 0;
-    for (int kt = 0; kt < p.KT; ++kt) {
-      const int s = kt % STAGES;
-      const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-      if (kt >= STAGES && !mbar_wait(bars + 8 * (STAGES + s), ph ^ 1u)) {
-        atomicCAS(&g_tc_status, 0, 1);
-        break;
+    long long g = 0;  // K blocks issued by this CTA
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      int tm, tn;
+      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      for (int kt = 0; kt < p.KT; ++kt, ++g) {
+        const int s = (int)(g % STAGES);
+        const uint32_t ph = (uint32_t)(g / STAGES) & 1u;
+        if (g >= STAGES && !mbar_wait(bars + 8 * (STAGES + s), ph ^ 1u)) {
+          atomicCAS(&g_tc_status, 0, 1);
+          ok = false;
+          break;
+        }
+        const uint32_t st = base + s * STAGE_BYTES;
+        const uint32_t full = bars + 8 * s;
+        mbar_expect_tx(full, STAGE_BYTES);
+        tma_load_2d(st, &map_ah, kt * BK, tm * BM, full);
+        tma_load_2d(st + A_TILE, &map_al, kt * BK, tm * BM, full);
+        tma_load_2d(st + 2 * A_TILE, &map_bh, kt * BK, tn * BN, full);
+        tma_load_2d(st + 2 * A_TILE + B_TILE, &map_bl, kt * BK, tn * BN, full);
       }
-      const uint32_t st = base + s * STAGE_BYTES;
-      const uint32_t full = bars + 8 * s;
-      mbar_expect_tx(full, STAGE_BYTES);
-      tma_load_2d(st, &map_ah, kt * BK, tm * BM, full);
-      tma_load_2d(st + TILE_BYTES, &map_al, kt * BK, tm * BM, full);
-      tma_load_2d(st + 2 * TILE_BYTES, &map_bh, kt * BK, tn * BN, full);
-      tma_load_2d(st + 3 * TILE_BYTES, &map_bl, kt * BK, tn * BN, full);
-      issued = kt + 1;
     }
     // Before this thread may leave, the last loads it issued into each stage must have
     // landed (normally long done: the MMA thread consumed them).
-    for (int kt = issued - 1; kt >= 0 && kt >= issued - STAGES; --kt)
-      mbar_wait(bars + 8 * (kt % STAGES), (uint32_t)(kt / STAGES) & 1u);
+    for (long long k = g - 1; k >= 0 && k >= g - STAGES; --k)
+      mbar_wait(bars + 8 * (int)(k % STAGES), (uint32_t)(k / STAGES) & 1u);
   } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    for (int kt = 0; kt < p.KT; ++kt) {
-      const int s = kt % STAGES;
-      const uint32_t ph = (uint32_t)(kt / STAGES) & 1u;
-      if (!mbar_wait(bars + 8 * s, ph)) {
+    // ---- MMA issuer: tile i accumulates into TMEM columns (i & 1) * ACC_COLS
+    long long g = 0;
+    bool ok = true;
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      if (i >= 2 && !mbar_wait(acc_empty + 8 * b, ((uint32_t)(i >> 1) & 1u) ^ 1u)) {
         atomicCAS(&g_tc_status, 0, 2);
         break;
       }
       tc_fence_after();
-      const uint32_t st = base + s * STAGE_BYTES;
+      const uint32_t acc = tmem + (uint32_t)b * ACC_COLS;
+      for (int kt = 0; kt < p.KT; ++kt, ++g) {
+        const int s = (int)(g % STAGES);
+        if (!mbar_wait(bars + 8 * s, (uint32_t)(g / STAGES) & 1u)) {
+          atomicCAS(&g_tc_status, 0, 2);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = base + s * STAGE_BYTES;
 #pragma unroll
-      for (int kk = 0; kk < BK / 8; ++kk) {
-        const uint64_t ah = sw128_desc(st + kk * 32);
-        const uint64_t al = sw128_desc(st + TILE_BYTES + kk * 32);
-        const uint64_t bh = sw128_desc(st + 2 * TILE_BYTES + kk * 32);
-        const uint64_t bl = sw128_desc(st + 3 * TILE_BYTES + kk * 32);
-        // small correction terms first, then the main product
-        mma_tf32(tmem, al, bh, (kt | kk) != 0 ? 1u : 0u);
-        mma_tf32(tmem, ah, bl, 1u);
-        mma_tf32(tmem, ah, bh, 1u);
+        for (int kk = 0; kk < BK / 8; ++kk) {
+          const uint64_t ah = sw128_desc(st + kk * 32);
+          const uint64_t al = sw128_desc(st + A_TILE + kk * 32);
+          const uint64_t bh = sw128_desc(st + 2 * A_TILE + kk * 32);
+          const uint64_t bl = sw128_desc(st + 2 * A_TILE + B_TILE + kk * 32);
+          // small correction terms first, then the main product
+          mma_tf32(acc, al, bh, (kt | kk) != 0 ? 1u : 0u);
+          mma_tf32(acc, ah, bl, 1u);
+          mma_tf32(acc, ah, bh, 1u);
+        }
+        mma_commit(bars + 8 * (STAGES + s));  // stage s free once these MMAs complete
       }
-      mma_commit(bars + 8 * (STAGES + s));  // stage s free once these MMAs complete
+      if (ok) mma_commit(acc_full + 8 * b);  // accumulator b complete
     }
-    mma_commit(accum_bar);  // accumulator complete once every MMA above has completed
-  }
-  __syncwarp();
-
-  // ---- epilogue: warp w owns TMEM lanes (tile rows) 32w .. 32w + 31
-  const bool ready = __all_sync(0xffffffffu, mbar_wait(accum_bar, 0));  // warp-uniform
-  if (!ready && lane == 0) atomicCAS(&g_tc_status, 0, 3);
-  tc_fence_after();
-  if (ready) {
-    const int row = tm * BM + warp * 32 + lane;
-    const int col0 = tn * BN;
-    float *crow = p.C + (long long)row * p.ldc + col0;
+  } else if (warp >= 2) {
+    // ---- epilogue: warp w reads TMEM lane quadrant w % 4 = tile rows 32 (w % 4) .. + 31
+    const int q = warp & 3;
+    float *buf = epi + (warp - 2) * 32 * EPI_PITCH;
+    int i = 0;
+    for (int t = blockIdx.x; t < tiles; t += gridDim.x, ++i) {
+      const int b = i & 1;
+      const bool ready =
+          __all_sync(0xffffffffu, mbar_wait(acc_full + 8 * b, (uint32_t)(i >> 1) & 1u));
+      if (!ready) {
+        if (lane == 0) atomicCAS(&g_tc_status, 0, 3);
+        break;
+      }
+      tc_fence_after();
+      int tm, tn;
+      tile_coords(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+      const int row0 = tm * BM + q * 32;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)c, v);
-      if (row < p.M) {
-        const int nvalid = p.N - (col0 + c);
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld32(tmem + (uint32_t)b * ACC_COLS + ((uint32_t)(q * 32) << 16) + (uint32_t)c, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j < nvalid) {
-            const float acc = __uint_as_float(v[j]);
-            crow[c + j] = (p.beta != 0.0f) ? fmaf(p.alpha, acc, p.beta * crow[c + j])
-                                           : p.alpha * acc;
+        for (int j = 0; j < 32; ++j) buf[lane * EPI_PITCH + j] = __uint_as_float(v[j]);
+        __syncwarp();
+        // lane l now writes column c + l of the warp's 32 rows: 128-byte row segments
+        const int col = tn * BN + c + lane;
+        if (col < p.N) {
+#pragma unroll 4
+          for (int r = 0; r < 32; ++r) {
+            const int row = row0 + r;
+            if (row < p.M) {
+              float *dst = p.C + (long long)row * p.ldc + col;
+              const float accv = buf[r * EPI_PITCH + lane];
+              *dst = (p.beta != 0.0f) ? fmaf(p.alpha, accv, p.beta * *dst) : p.alpha * accv;
+            }
           }
         }
+        __syncwarp();
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty + 8 * b);  // accumulator b may be reused
     }
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TMEM_COLS);
@@ -322,10 +373,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 // ------------------------------------------------------------------------------------
 // Host side
 
-// Tensor map of a rows x cols row-major FP32 matrix (ld = cols, cols % 32 == 0), 32 x 128
-// boxes (32 along the contiguous dimension), 128-byte swizzle.
-static bool make_map(CUtensorMap *map, const float *ptr, long long rows, long long cols) {
-  return encode_map_2d(map, ptr, rows, cols, cols, BK, BM, true);
+// Tensor map of a rows x cols row-major FP32 matrix (ld = cols, cols % 32 == 0), boxes of
+// 32 (along the contiguous dimension) x box_rows, 128-byte swizzle.
+static bool make_map(CUtensorMap *map, const float *ptr, long long rows, long long cols,
+                     int box_rows) {
+  return encode_map_2d(map, ptr, rows, cols, cols, BK, box_rows, true);
 }
 
 struct Shape {
@@ -453,8 +505,10 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
   e = cudaGetLastError();
   if (e == cudaSuccess) {
     CUtensorMap m_ah, m_al, m_bh, m_bl;
-    if (!tc::make_map(&m_ah, ah, sh.Mp, sh.Kp) || !tc::make_map(&m_al, al, sh.Mp, sh.Kp) ||
-        !tc::make_map(&m_bh, bh, sh.Np, sh.Kp) || !tc::make_map(&m_bl, bl, sh.Np, sh.Kp)) {
+    if (!tc::make_map(&m_ah, ah, sh.Mp, sh.Kp, tc::BM) ||
+        !tc::make_map(&m_al, al, sh.Mp, sh.Kp, tc::BM) ||
+        !tc::make_map(&m_bh, bh, sh.Np, sh.Kp, tc::BN) ||
+        !tc::make_map(&m_bl, bl, sh.Np, sh.Kp, tc::BN)) {
       e = cudaErrorInvalidValue;
     } else {
       tc::Params p;
@@ -468,8 +522,10 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
       p.beta = beta;
       p.C = C;
       p.ldc = ldc;
-      tc::tc3_kernel<<<(unsigned)(tiles_m * tiles_n), tc::THREADS, tc::SMEM_BYTES, stream>>>(
-          m_ah, m_al, m_bh, m_bl, p);
+      // persistent: one CTA per SM (or per tile when there are fewer tiles)
+      const long long grid = std::min<long long>(tiles_m * tiles_n, num_sms);
+      tc::tc3_kernel<<<(unsigned)grid, tc::THREADS, tc::SMEM_BYTES, stream>>>(m_ah, m_al,
+                                                                            m_bh, m_bl, p);
       e = cudaGetLastError();
     }
   }
