@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import argparse
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -65,21 +66,34 @@ def parse():
 
 
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "sgemm_ffma_traffic.json")
-KERNEL_SOURCES = ("dense_fp32_matrix_08_gb300/csrc", "include")
+CSRC = os.path.join(ROOT, "dense_fp32_matrix_08_gb300", "csrc")
+KERNEL_TU = "sgemm_tma.cu"  # the dominant kernel's translation unit
+KERNEL_HOST = ("sgemm_plan.h", "sgemm_api.cu")  # the host code that plans and launches it
+
+
+def kernel_sources():
+    """The files the dominant GEMM kernel and its launch come from: its translation unit with
+    every local header it includes, transitively, and the planning/launch host files."""
+    seen, todo = [], [KERNEL_TU]
+    while todo:
+        fn = todo.pop(0)
+        if fn in seen or not os.path.exists(os.path.join(CSRC, fn)):
+            continue
+        seen.append(fn)
+        with open(os.path.join(CSRC, fn)) as f:
+            todo += re.findall(r'^\s*#\s*include\s+"([^"/]+)"', f.read(), re.M)
+    return sorted(set(seen) | set(KERNEL_HOST))
 
 
 def kernel_source_hash() -> str:
-    """sha256 over the library's CUDA/C++ sources and headers: a recorded ncu traffic figure
-    is only reported while this hash matches the one it was taken with."""
+    """sha256 over kernel_sources(): a recorded ncu traffic figure is only reported while
+    this hash matches the one it was taken with (changes to other kernels leave it valid)."""
     import hashlib
     h = hashlib.sha256()
-    for d in KERNEL_SOURCES:
-        full = os.path.join(ROOT, d)
-        for fn in sorted(os.listdir(full)):
-            if fn.endswith((".cu", ".cuh", ".h")):
-                h.update(fn.encode())
-                with open(os.path.join(full, fn), "rb") as f:
-                    h.update(f.read())
+    for fn in kernel_sources():
+        h.update(fn.encode())
+        with open(os.path.join(CSRC, fn), "rb") as f:
+            h.update(f.read())
     return h.hexdigest()
 
 
