@@ -42,9 +42,12 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},
     VariantKernels{},  // TMA-fed thin-M and thin-N kernels (sgemm_thin.cu)
     VariantKernels{},
+    VariantKernels{},  // cluster thin-M and thin-N kernels (sgemm_thin.cu)
+    VariantKernels{},
 };
 static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
-                  kThinNVariant == 34 && kThinTmaVariant == 41 && kNumVariants == 43,
+                  kThinNVariant == 34 && kThinTmaVariant == 41 &&
+                  kThinClusterVariant == 43 && kNumVariants == 45,
               "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).
@@ -240,7 +243,10 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     tp.vec_c = vec_c ? 1 : 0;
     cudaError_t te;
     int parts = pl.split;  // partial tiles per C tile for the reduce kernel
-    if (vs.thin >= 3) {
+    if (vs.thin >= 5) {
+      te = launch_thin_cluster(vs.thin == 6, tp, status_word(), stream);
+      parts = 1;  // the cluster adds its slices itself
+    } else if (vs.thin >= 3) {
       te = launch_thin_tma(vs.thin == 4, tp, status_word(), stream);
     } else {
       // 128-bit loads of the streamed operand: B rows (thin-M) or A rows (thin-N)
@@ -387,6 +393,7 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
+  thin_cluster_capacity(pr.cluster_ctas);
   Plan pl = (force_v < 0 && force_split == 0)
                 ? automatic_plan(pr, alpha, beta, num_sms)
                 : cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
@@ -492,9 +499,10 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
   pr.b_tma = ldb % 4 == 0;
   int rc = validate(pr, alpha, true, true, true);
   if (rc != 0) return rc;
-  if (num_sms <= 0) {
+  if (num_sms <= 0) {  // the current device, with its own cluster capacity
     cudaError_t e = device_setup(&num_sms);
     if (e != cudaSuccess) return (int)e;
+    thin_cluster_capacity(pr.cluster_ctas);
   }
   Plan pl;
   if (M == 0 || N == 0) {

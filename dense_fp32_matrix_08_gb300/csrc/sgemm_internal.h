@@ -43,6 +43,13 @@ cudaError_t launch_thin(bool thin_m, const thin::ThinParams &p, bool vec, cudaSt
 // TMA-addressable); p.split CTAs along K, p.k_per_split a multiple of 8, at most 1024.
 cudaError_t launch_thin_tma(bool thin_n, const thin::ThinParams &p, int *status,
                             cudaStream_t stream);
+// Cluster thin kernel (sgemm_thin_cluster.cuh): thin-M (A and B TMA-addressable) or thin-N;
+// p.split = the cluster size (1, 2, 4 or 8), p.k_per_split a multiple of 8. No workspace.
+cudaError_t launch_thin_cluster(bool thin_n, const thin::ThinParams &p, int *status,
+                                cudaStream_t stream);
+// CTAs of the cluster thin kernel resident at once on the current device in clusters of
+// 1, 2, 4 and 8 (zeros if unknown).
+void thin_cluster_capacity(int ctas[4]);
 
 // TMA-fed GEMM (sgemm_ffma_tma.cuh): one-time kernel attributes for the current device, and
 // a launch of instance `inst` (VariantShape::inst) on row-major A (lda) and B (ldb); for

@@ -23,6 +23,9 @@ struct Problem {
                                // A_st is the k-major A the at variants read, no copy needed
   bool kpair_ok = false;       // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
   bool b_kmajor = false;       // op(B) = B_st^T with B_st 16-byte aligned, ldb % 4 == 0
+  // CTAs of the cluster thin kernel that the device holds at once in clusters of 1, 2, 4
+  // and 8 (queried from the driver; 0 = unknown, modelled by cluster_ctas_model)
+  int cluster_ctas[4] = {0, 0, 0, 0};
 };
 
 // Shape of one compiled tile configuration (mirrors TileConfig in sgemm_ffma.cuh).
@@ -35,7 +38,8 @@ struct VariantShape {
   bool kpair = false;  // the K-paired TMA-fed kernel (sgemm_ffma_kpair.cuh): K-major B
   int inst = 0;        // TMA-fed kernels: instance index of the launcher (sgemm_tma.cu)
   int thin = 0;        // streaming kernels: 1 thin-M, 2 thin-N (sgemm_thin.cuh), 3 TMA-fed
-                       // thin-M, 4 TMA-fed thin-N (sgemm_thin_tma.cuh)
+                       // thin-M, 4 TMA-fed thin-N (sgemm_thin_tma.cuh), 5 cluster thin-M,
+                       // 6 cluster thin-N (sgemm_thin_cluster.cuh)
   bool at = false;     // TMA-fed kernel reading A k-major (A^T; copied first if row-major)
   int twin = -1;       // at variants: the variant with the same tiles and arithmetic that
                        // transposes A in shared memory instead (bitwise the same result)
@@ -109,6 +113,12 @@ constexpr VariantShape kVariants[] = {
     // 42: TMA-fed thin-N (C^T = B^T A^T on the same kernel): 256 x 16 C tiles, A streamed
     // as [256 m][8 k] chunks
     {256, 16, 8, 256, 8, 16, 2, 1, 1, 0, 0.7, true, false, false, false, 0, 4},
+    // 43, 44: cluster thin-M / thin-N: 16 x 128 (128 x 16) C tiles, 8 warps streaming both
+    // operands by TMA in 8-k chunks (16 x 4 outputs per lane, every warp over the whole
+    // tile), the K slices of a tile one cluster of 1, 2, 4 or 8 CTAs reduced through
+    // distributed shared memory (no workspace, one launch)
+    {16, 128, 8, 256, 16, 4, 4, 1, 1, 0, 0.8, true, false, false, false, 0, 5},
+    {128, 16, 8, 256, 4, 16, 4, 1, 1, 0, 0.8, true, false, false, false, 0, 6},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;
@@ -117,6 +127,8 @@ constexpr int kThinMVariant = 33, kThinNVariant = 34;
 constexpr int kThinMaxDim = 64;  // thin kernels considered for M (thin-M) or N (thin-N) <= this
 constexpr int kThinMKmax = 512, kThinNKmax = 2048;  // K slice bounds (shared memory)
 constexpr int kThinTmaVariant = 41, kThinTmaKmax = 1024;
+constexpr int kThinClusterVariant = 43;  // 43 thin-M, 44 thin-N
+constexpr int kMaxThinCluster = 8;
 static_assert(kVariants[kTmaVariant].tma, "TMA variant index");
 static_assert(kVariants[kFirstKpairVariant].kpair, "K-paired variant index");
 
@@ -147,49 +159,75 @@ struct Plan {
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+// CTAs of the cluster thin kernel resident at once in clusters of S = 1 << l2 CTAs: the
+// driver's figure when known, else a model of a GPU whose SMs sit in GPCs of about 19 SMs
+// (a cluster never spans two): GB300 holds 144 CTAs in clusters of 4 and 120 in clusters of 8.
+inline long long cluster_ctas(const Problem &p, int num_sms, int l2) {
+  if (p.cluster_ctas[l2] > 0) return p.cluster_ctas[l2];
+  static const double kFill[4] = {1.0, 1.0, 18.0 / 19.0, 15.0 / 19.0};
+  const int S = 1 << l2;
+  return std::max<long long>(S, (long long)(num_sms * kFill[l2]) / S * S);
+}
+
 // Modelled cost of a thin-product streaming kernel (variant v with s.thin != 0) with `split`
-// K slices. Both kernels stream one operand once and are bound by HBM at their shapes:
+// K slices. The kernels stream one operand once and are bound by HBM at their shapes:
 // the cost is the larger of the streamed bytes at ~2800 bytes/cycle for the chip (about
 // 80% of the measured copy bandwidth) and the FMA work at the variant's efficiency, plus
-// ~2000 cycles per launch. Partial tiles add their write and the reduce's read.
+// ~2000 cycles per launch. Partial tiles add their write and the reduce's read. The cluster
+// kernels (thin 5, 6) take split = the cluster size (1, 2, 4 or 8), have no K bound and no
+// partial tiles, and fill HBM once about 85% of the SMs stream (a TMA streaming probe
+// reached the full copy bandwidth from 128 of 152 SMs).
 inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool beta_nz) {
   const VariantShape &s = kVariants[v];
   Plan pl;
   pl.variant = v;
   pl.tiles_m = (int)ceil_div(p.M, s.BM);
   pl.tiles_n = (int)ceil_div(p.N, s.BN);
-  const int kmax = s.thin == 1 ? kThinMKmax : s.thin == 2 ? kThinNKmax : kThinTmaKmax;
-  const bool streams_b = s.thin == 1 || s.thin == 3;  // thin-M kinds stream B, thin-N A
+  const bool cluster = s.thin >= 5;
+  const bool streams_b = s.thin == 1 || s.thin == 3 || s.thin == 5;  // thin-M kinds stream B
   const int kq = 8;  // K slice granule (the load batch / TMA chunk of the thin kernels)
   long long kps = ceil_div(ceil_div(p.K, std::max(1, split)), kq) * kq;
-  kps = std::min<long long>(std::max<long long>(kps, kq), kmax);
-  split = (int)ceil_div(p.K, kps);
+  if (cluster) {
+    int l2 = 0;
+    while ((1 << l2) < split && l2 < 3) ++l2;
+    split = 1 << l2;
+    kps = std::max<long long>(kps, kq);
+  } else {
+    const int kmax = s.thin == 1 ? kThinMKmax : s.thin == 2 ? kThinNKmax : kThinTmaKmax;
+    kps = std::min<long long>(std::max<long long>(kps, kq), kmax);
+    split = (int)ceil_div(p.K, kps);
+  }
   const long long tiles = (long long)pl.tiles_m * pl.tiles_n;
   const long long ctas = tiles * split;
   const double per_cta_fma = (double)s.BM * s.BN * (double)kps;
   const double rate = 128.0 * s.eff / s.min_blocks;  // FMA per cycle per resident CTA
-  const long long slots = (long long)num_sms * s.min_blocks;
-  const double compute = (double)ceil_div(ctas, slots) * per_cta_fma / rate;
+  int l2 = 0;
+  while ((1 << l2) < split) ++l2;
+  const long long slots = cluster ? std::min<long long>(num_sms, cluster_ctas(p, num_sms, l2))
+                                  : (long long)num_sms * s.min_blocks;
+  const long long waves = ceil_div(ctas, slots);
+  const double compute = (double)waves * per_cta_fma / rate;
   // streamed operand once per tile row (thin-M: B per row block) or column (thin-N: A)
   const double streamed = streams_b ? 4.0 * pl.tiles_m * (double)p.K * p.N
                                     : 4.0 * pl.tiles_n * (double)p.M * p.K;
   const double small = streams_b ? 4.0 * (double)p.M * p.K : 4.0 * (double)p.K * p.N;
-  const int groups = split;  // partial tiles per C tile
+  const int groups = cluster ? 1 : split;  // partial tiles per C tile in the workspace
   const double part = groups > 1 ? (double)tiles * groups * s.BM * s.BN * 4.0 : 0.0;
   const double mn_c = (double)p.M * p.N * 4.0 * (beta_nz ? 2.0 : 1.0);
   const double bytes = streamed + small + mn_c + 2.0 * part;
   pl.main_tiles = 0;
   pl.split = split;
-  pl.k_per_split = (int)kps;
+  pl.k_per_split = (int)std::min<long long>(kps, 0x7ffffff8LL);
   pl.group_m = 1;
   pl.ctas = (int)std::min<long long>(ctas, 0x7fffffffLL);
   pl.launches = groups > 1 ? 2 : 1;
   pl.ws_bytes = groups > 1 ? (size_t)part : 0;
-  // HBM is streamed at full speed only while every SM has work: scale the bandwidth by the
-  // average fraction of CTA slots the grid fills over its waves. Each wave also pays ~3000
-  // cycles of start-up (first copies in flight, staging) and reduction that nothing hides.
-  const long long waves = ceil_div(ctas, slots);
-  const double fill = (double)ctas / (double)(waves * slots);
+  // HBM is streamed at full speed only while enough SMs have work: scale the bandwidth by
+  // the average fraction of CTA slots the grid fills over its waves (cluster kernels: of
+  // 85% of the SMs). Each wave also pays ~3000 cycles of start-up (first copies in flight,
+  // staging) and reduction that nothing hides.
+  const double fill = cluster ? std::min(1.0, (double)ctas / (double)waves / (0.85 * num_sms))
+                              : (double)ctas / (double)(waves * slots);
   pl.cycles = std::max(compute, bytes / (2800.0 * fill)) + 3000.0 * (double)waves +
               2000.0 * pl.launches;
   if (ctas > 0x7fffffffLL || pl.tiles_m > 65535 || pl.tiles_n > 65535 || split > 65535)
@@ -419,10 +457,23 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
         ((s.BM <= 16 && p.b_tma && !p.transa) || (s.BN <= 16 && p.a_tma && !p.transb)))
       continue;
     if (s.thin) {
-      const bool thin_n_kind = s.thin == 2 || s.thin == 4;
+      const bool thin_n_kind = s.thin == 2 || s.thin == 4 || s.thin == 6;
       if (force_v < 0 && (thin_n_kind ? p.N : p.M) > kThinMaxDim) continue;
       if (s.thin == 3 && (!p.b_tma || p.transa)) continue;  // B read by TMA as stored
       if (s.thin == 4 && (!p.a_tma || p.transb)) continue;  // A read by TMA as stored
+      if (s.thin >= 5) {  // cluster kernels: both operands read by TMA as stored
+        if (!p.a_tma || !p.b_tma || p.transa || p.transb) continue;
+        if (force_split >= 1) {
+          consider(model_thin(p, v, std::min(force_split, kMaxThinCluster), num_sms, beta_nz));
+          continue;
+        }
+        for (int sp = 1; sp <= kMaxThinCluster; sp *= 2) {
+          const long long kps = ceil_div(ceil_div(p.K, sp), 8) * 8;
+          if (sp > 1 && (long long)(sp - 1) * kps >= p.K) break;  // no empty K slices
+          consider(model_thin(p, v, sp, num_sms, beta_nz));
+        }
+        continue;
+      }
       const int kmax = s.thin == 1 ? kThinMKmax : s.thin == 2 ? kThinNKmax : kThinTmaKmax;
       const int min_split = (int)ceil_div(p.K, kmax);
       if (force_split >= 1) {

@@ -101,6 +101,7 @@ int sgemm_f32_autotune(int transa, int transb, int M, int N, int K, float alpha,
   int num_sms = 0;
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
+  thin_cluster_capacity(pr.cluster_ctas);
   const bool beta_nz = beta != 0.0f;
 
   // Candidates: every configuration with the model's split choice, no split, and whole
@@ -113,7 +114,8 @@ int sgemm_f32_autotune(int transa, int transb, int M, int N, int K, float alpha,
   std::vector<Cand> cands;
   double best_model = std::numeric_limits<double>::infinity();
   for (int v = 0; v < kNumVariants; ++v)
-    for (int s : {0, 1, -1}) {
+    for (int s : {0, 1, -1, 2, 4, 8}) {
+      if (s > 1 && kVariants[v].thin < 5) continue;  // cluster sizes of the cluster kernels
       const Plan pl = make_plan(pr, alpha, beta, num_sms, v, s);
       if (pl.variant < 0 || !(pl.cycles < std::numeric_limits<double>::infinity())) continue;
       bool dup = false;

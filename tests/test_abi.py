@@ -82,7 +82,7 @@ def test_variant_table():
         assert info["TM"] * info["TN"] >= 16 and info["threads"] % 32 == 0
         # the CTA tile is exactly covered by its threads' accumulator tiles, once, or once
         # per k-group where several thread groups split the CTA's K range (thin-M: 4 groups,
-        # or 8 warps that each take 4 of every stage's 32 k rows)
+        # or 8 warps that each take 4 of every stage's 32 k rows, or every 8th 8-k chunk)
         covered = info["threads"] * info["TM"] * info["TN"]
         assert covered % (info["BM"] * info["BN"]) == 0
         assert covered // (info["BM"] * info["BN"]) in (1, 4, 8)
@@ -105,13 +105,18 @@ def test_plan_headline_uses_large_tiles():
     assert p["launches"] == pre + (2 if p["split"] > 1 else 1)
 
 
+THIN_CLUSTER = (43, 44)  # K slices reduced inside a cluster: no workspace, one launch
+
+
 def test_plan_thin_shapes_use_thin_tiles_and_split_k():
-    p = _plan(16, 4096, 4096)
-    info = sg.sgemm_f32_variant_info(p["variant"])
-    assert info["BM"] <= 16 and p["split"] > 1 and p["ws_bytes"] > 0
-    p = _plan(4096, 16, 8192)
-    info = sg.sgemm_f32_variant_info(p["variant"])
-    assert info["BN"] <= 16 and p["split"] > 1
+    for M, N, K in ((16, 4096, 4096), (4096, 16, 8192)):
+        p = _plan(M, N, K)
+        info = sg.sgemm_f32_variant_info(p["variant"])
+        assert min(info["BM"], info["BN"]) <= 16 and p["split"] > 1
+        if p["variant"] in THIN_CLUSTER:
+            assert p["split"] in (2, 4, 8) and p["ws_bytes"] == 0 and p["launches"] == 1
+        else:
+            assert p["ws_bytes"] > 0
 
 
 TMA_VARIANTS = (26, 30, 31, 32, 37, 38)  # TMA-fed, A as stored (aligned copies if needed)
@@ -140,7 +145,9 @@ def test_plan_workspace_formula():
             pre, copies = pre + r256(4 * M * (-(-K // 4) * 4)), copies + 1
         if p["variant"] in TMA_VARIANTS + AT_VARIANTS and N % 4:
             pre, copies = pre + r256(4 * K * (-(-N // 4) * 4)), copies + 1
-        if p["split"] > 1:
+        if p["variant"] in THIN_CLUSTER:
+            assert p["ws_bytes"] == 0 and p["launches"] == 1
+        elif p["split"] > 1:
             assert split_tiles > 0 and p["launches"] == 2 + copies
             assert p["ws_bytes"] == pre + 4 * p["split"] * split_tiles * info["BM"] * info["BN"]
         else:

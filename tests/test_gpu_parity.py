@@ -15,12 +15,14 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 43  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 45  # compiled tile configurations; checked against the library below
 TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
 THIN_M_TMA = 41  # TMA-fed thin-M: B must be TMA-addressable
 THIN_N_TMA = 42  # TMA-fed thin-N: A must be TMA-addressable
+THIN_M_CL, THIN_N_CL = 43, 44  # cluster thin kernels: A and B must be TMA-addressable
+TMA_THIN = (THIN_M_TMA, THIN_N_TMA, THIN_M_CL, THIN_N_CL)
 
 if torch.cuda.is_available():
     import dense_fp32_matrix_08_gb300 as sg
@@ -110,11 +112,11 @@ RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
-    if not aligned and variant in (THIN_M_TMA, THIN_N_TMA):
-        pytest.skip("the TMA-fed thin kernels read the streamed operand by TMA: aligned only")
+    if not aligned and variant in TMA_THIN:
+        pytest.skip("the TMA-fed thin kernels read their operands by TMA: aligned only")
     for (M, N, K) in RAGGED:
         A, B, C = make_inputs(M, N, K, seed=M * 7 + N * 3 + K)
-        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS + (THIN_M_TMA, THIN_N_TMA):
+        if aligned and variant in TMA_VARIANTS + KPAIR_VARIANTS + TMA_THIN:
             # TMA needs ld % 4 == 0: pad the rows
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
         elif variant in KPAIR_VARIANTS:  # aligned A; B and C with odd ld and offsets
@@ -162,7 +164,7 @@ THIN_N_SHAPES = [(1, 1, 1), (255, 5, 7), (1024, 16, 2049), (1000, 16, 4100), (41
                  (3000, 16, 1100)]
 
 
-@pytest.mark.parametrize("kind", ["m", "n", "mt", "nt"])
+@pytest.mark.parametrize("kind", ["m", "n", "mt", "nt", "mc", "nc"])
 @pytest.mark.parametrize("split", [0, 1, 5, 17])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_thin_kernels(kind, split, aligned):
@@ -170,11 +172,14 @@ def test_thin_kernels(kind, split, aligned):
     K slices that are not a multiple of the 8-deep load batch, column quads and rows that
     cross N and M, one slice (alpha / beta in the kernel) and several (reduce kernel).
     The TMA-fed thin-M kernel ("mt") needs an aligned B; split 17 on K = 2049 / 1100 gives
-    slices that end inside a 32-row B tile."""
-    if kind in ("mt", "nt") and not aligned:
-        pytest.skip("the TMA-fed thin kernels read the streamed operand by TMA: aligned only")
-    variant = {"m": THIN_M, "n": THIN_N, "mt": THIN_M_TMA, "nt": THIN_N_TMA}[kind]
-    for (M, N, K) in (THIN_N_SHAPES if kind in ("n", "nt") else THIN_M_SHAPES):
+    slices that end inside a 32-row B tile. The cluster kernels ("mc", "nc") take the split
+    as their cluster size, rounded up to 1, 2, 4 or 8 (5 and 17 give 8: on K = 1 and 7 most
+    of the cluster's K slices are empty)."""
+    if kind in ("mt", "nt", "mc", "nc") and not aligned:
+        pytest.skip("the TMA-fed thin kernels read their operands by TMA: aligned only")
+    variant = {"m": THIN_M, "n": THIN_N, "mt": THIN_M_TMA, "nt": THIN_N_TMA,
+               "mc": THIN_M_CL, "nc": THIN_N_CL}[kind]
+    for (M, N, K) in (THIN_N_SHAPES if kind in ("n", "nt", "nc") else THIN_M_SHAPES):
         A, B, C = make_inputs(M, N, K, seed=M + 3 * N + 5 * K + split)
         if aligned:
             lds, offs = (-(-K // 4) * 4, -(-N // 4) * 4, None), (0, 0, 0)
@@ -184,6 +189,31 @@ def test_thin_kernels(kind, split, aligned):
         assert guard, (M, N, K)
         R, S = oracle.sgemm_f64(A, B, C, 0.75, -1.25)
         assert_bound(out.numpy(), R, S, -1.25, C.numpy(), f"thin-{kind} s{split} {M,N,K}")
+
+
+CLUSTER_SHAPES = [(16, 4096, 1000), (40, 1000, 777), (16, 129, 4104), (3, 4100, 4096)]
+
+
+@pytest.mark.parametrize("thin_n", [False, True])
+@pytest.mark.parametrize("cluster", [1, 2, 4, 8])
+@pytest.mark.parametrize("beta", [0.0, 2.0])
+def test_thin_cluster_sizes(thin_n, cluster, beta):
+    """The cluster thin kernels at every cluster size: several small blocks (M = 40 is 3 row
+    blocks), wide extents that end inside a 128-wide tile, K slices that end inside an 8-k
+    chunk, beta = 0 and beta != 0, and no write outside the C view. The result is
+    bitwise the same on a second run (fixed-order sums within and across the cluster)."""
+    for (M, N, K) in CLUSTER_SHAPES:
+        if thin_n:
+            M, N = N, M
+        A, B, C = make_inputs(M, N, K, seed=M + 7 * N + 11 * K + cluster)
+        lds = (-(-K // 4) * 4, -(-N // 4) * 4, None)
+        v = THIN_N_CL if thin_n else THIN_M_CL
+        out, guard = _run(A, B, C, 1.5, beta, *lds, variant=v, split=cluster)
+        assert guard, (M, N, K)
+        R, S = oracle.sgemm_f64(A, B, C, 1.5, beta)
+        assert_bound(out.numpy(), R, S, beta, C.numpy(), f"v{v} S{cluster} {M,N,K}")
+        again, _ = _run(A, B, C, 1.5, beta, *lds, variant=v, split=cluster)
+        assert torch.equal(out, again), (M, N, K)
 
 
 # --------------------------------------------------------------------------------------
