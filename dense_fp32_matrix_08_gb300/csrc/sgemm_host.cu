@@ -2,9 +2,12 @@
 // runs on the GPU in row blocks; the host <-> device copies of one block overlap the
 // computation of its neighbours:
 //
-//   copy-in stream   B   A0 C0   A1 C1   .......  A2 C2 (after D2H 0) ...
-//   compute stream             GEMM 0    GEMM 1    GEMM 2 ...
-//   copy-out stream                      C0 out    C1 out   ...
+//   copy-in stream   B/A0 chunk 0, 1, ... C0   A1 C1   .......  A2 C2 (after D2H 0) ...
+//   compute stream     GEMM 0 chunk 0, 1, ...  +C0   GEMM 1    GEMM 2 ...
+//   copy-out stream                               C0 out    C1 out   ...
+//
+// With a large B the first block is computed in K chunks as B and A0 arrive (see below), so
+// the GEMMs start after one chunk instead of all of B.
 //
 // Device buffers (B whole; A and C blocks, double-buffered) come from the library's
 // workspace pool on the caller's stream and go back to it when the work is done.
@@ -56,6 +59,27 @@ struct Events {
   }
 };
 
+// y += beta * x over n contiguous floats (both pool buffers, 256-byte aligned): the first
+// block's beta * C0 when that block is computed in K chunks.
+__global__ void add_scaled_kernel(float *__restrict__ y, const float *__restrict__ x,
+                                  long long n, float beta) {
+  const long long n4 = n / 4;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  float4 *y4 = reinterpret_cast<float4 *>(y);
+  const float4 *x4 = reinterpret_cast<const float4 *>(x);
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n4; i += stride) {
+    const float4 a = x4[i];
+    float4 b = y4[i];
+    b.x = fmaf(beta, a.x, b.x);
+    b.y = fmaf(beta, a.y, b.y);
+    b.z = fmaf(beta, a.z, b.z);
+    b.w = fmaf(beta, a.w, b.w);
+    y4[i] = b;
+  }
+  if (blockIdx.x == 0)
+    for (long long i = 4 * n4 + threadIdx.x; i < n; i += blockDim.x) y[i] = fmaf(beta, x[i], y[i]);
+}
+
 }  // namespace
 }  // namespace sgemm
 
@@ -93,11 +117,20 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
     if (bytes == 0 || e != cudaSuccess) return;
     e = cudaMallocFromPoolAsync(reinterpret_cast<void **>(p), bytes, pool, stream);
   };
+  // Head: with several blocks and a large B, block 0 is computed in K chunks as B arrives,
+  // C0 = alpha A0[:, k0:k1) B[k0:k1, :] + C0 chunk by chunk (the first chunk with beta 0),
+  // then C0 += beta * C0_old from a staging copy, so the GEMMs start after one small chunk
+  // of B and A0 instead of all of B and the C0 rows. The chunk boundaries round the running
+  // sum to FP32 once per chunk; the result stays within the library's bound, but is not
+  // bitwise the single-call result.
+  const bool chunk_head = reads_ab && blocks >= 2 && K >= 1024 && b_bytes >= ((size_t)32 << 20);
+  float *dCs = nullptr;  // staged C0 rows (chunked head with beta != 0)
   alloc(&dB, b_bytes);
   for (int q = 0; q < std::min(2, blocks); ++q) {
     alloc(&dA[q], a_bytes);
     alloc(&dC[q], c_bytes);
   }
+  if (chunk_head && need_c_in) alloc(&dCs, c_bytes);
   Events evs;
   cudaEvent_t ev_start = nullptr;
   if (e == cudaSuccess) e = evs.make(&ev_start);
@@ -120,19 +153,71 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
     if (e == cudaSuccess) e = cudaEventRecord(ev_in[i], s_in);
   };
 
-  if (e == cudaSuccess && reads_ab)
-    e = cudaMemcpy2DAsync(dB, (size_t)N * 4, B, (size_t)ldb * 4, (size_t)N * 4, K,
-                          cudaMemcpyHostToDevice, s_in);
-  copy_in(0);
+  std::vector<int> kb{0};  // chunk boundaries: a first chunk of 256, then about K / 8
+  if (chunk_head) {
+    const int kc = (int)std::min<long long>(K, ceil_div(ceil_div(K, 8), 128) * 128);
+    kb.push_back(std::min(K, 256));
+    while (kb.back() < K) kb.push_back(std::min(K, kb.back() + kc));
+  } else {
+    kb.push_back(K);
+  }
+  const int nchunks = (int)kb.size() - 1;
+  std::vector<cudaEvent_t> ev_chunk(chunk_head ? nchunks : 0, nullptr);
+  cudaEvent_t ev_c0 = nullptr;
+  if (chunk_head) {
+    const int rows0 = rows_of(0);
+    for (int c = 0; c < nchunks && e == cudaSuccess; ++c) {
+      const int k0 = kb[c], kn = kb[c + 1] - kb[c];
+      e = cudaMemcpy2DAsync(dB + (size_t)k0 * N, (size_t)N * 4, B + (long long)k0 * ldb,
+                            (size_t)ldb * 4, (size_t)N * 4, kn, cudaMemcpyHostToDevice, s_in);
+      if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(dA[0] + k0, (size_t)K * 4, A + k0, (size_t)lda * 4,
+                              (size_t)kn * 4, rows0, cudaMemcpyHostToDevice, s_in);
+      if (e == cudaSuccess) e = evs.make(&ev_chunk[c]);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_chunk[c], s_in);
+    }
+    if (need_c_in) {
+      if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(dCs, (size_t)N * 4, C, (size_t)ldc * 4, (size_t)N * 4, rows0,
+                              cudaMemcpyHostToDevice, s_in);
+      if (e == cudaSuccess) e = evs.make(&ev_c0);
+      if (e == cudaSuccess) e = cudaEventRecord(ev_c0, s_in);
+    }
+    if (e == cudaSuccess) ev_in[0] = ev_chunk[nchunks - 1];
+  } else {
+    if (e == cudaSuccess && reads_ab)
+      e = cudaMemcpy2DAsync(dB, (size_t)N * 4, B, (size_t)ldb * 4, (size_t)N * 4, K,
+                            cudaMemcpyHostToDevice, s_in);
+    copy_in(0);
+  }
   if (blocks > 1) copy_in(1);
   for (int i = 0; i < blocks && e == cudaSuccess; ++i) {
     const int r0 = i * mb, rows = rows_of(i);
-    e = cudaStreamWaitEvent(stream, ev_in[i], 0);
-    if (e != cudaSuccess) break;
-    // the block's product on the caller's stream, through the library's own entry point
-    rc = sgemm_f32(rows, N, K, alpha, reads_ab ? dA[i % 2] : nullptr, std::max(1, K),
-                   reads_ab ? dB : nullptr, N, beta, dC[i % 2], N, stream);
-    if (rc != 0) break;
+    if (i == 0 && chunk_head) {
+      for (int c = 0; c < nchunks && e == cudaSuccess && rc == 0; ++c) {
+        const int k0 = kb[c], kn = kb[c + 1] - kb[c];
+        e = cudaStreamWaitEvent(stream, ev_chunk[c], 0);
+        if (e == cudaSuccess)
+          rc = sgemm_f32(rows, N, kn, alpha, dA[0] + k0, K, dB + (size_t)k0 * N, N,
+                         c == 0 ? 0.0f : 1.0f, dC[0], N, stream);
+      }
+      if (e == cudaSuccess && rc == 0 && need_c_in) {
+        e = cudaStreamWaitEvent(stream, ev_c0, 0);
+        if (e == cudaSuccess) {
+          add_scaled_kernel<<<num_sms * 4, 256, 0, stream>>>(dC[0], dCs, (long long)rows * N,
+                                                              beta);
+          e = cudaGetLastError();
+        }
+      }
+      if (e != cudaSuccess || rc != 0) break;
+    } else {
+      e = cudaStreamWaitEvent(stream, ev_in[i], 0);
+      if (e != cudaSuccess) break;
+      // the block's product on the caller's stream, through the library's own entry point
+      rc = sgemm_f32(rows, N, K, alpha, reads_ab ? dA[i % 2] : nullptr, std::max(1, K),
+                     reads_ab ? dB : nullptr, N, beta, dC[i % 2], N, stream);
+      if (rc != 0) break;
+    }
     e = evs.make(&ev_done[i]);
     if (e == cudaSuccess) e = cudaEventRecord(ev_done[i], stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_done[i], 0);
@@ -161,7 +246,7 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
     if (evs.make(&j2) == cudaSuccess && cudaEventRecord(j2, s_out) == cudaSuccess)
       cudaStreamWaitEvent(stream, j2, 0);
   }
-  for (float *p : {dB, dA[0], dA[1], dC[0], dC[1]})
+  for (float *p : {dB, dA[0], dA[1], dC[0], dC[1], dCs})
     if (p != nullptr) {
       const cudaError_t f = cudaFreeAsync(p, stream);
       if (e == cudaSuccess) e = f;

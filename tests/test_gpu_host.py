@@ -27,7 +27,10 @@ def _host_view(x: torch.Tensor, ld: int, pinned: bool) -> torch.Tensor:
     return buf, view
 
 
-@pytest.mark.parametrize("shape", [(300, 200, 100), (5000, 700, 300), (9000, 64, 50)])
+# (4200, 2048, 4100): two row blocks and a 33.6 MB B, so the first block runs in K chunks
+# of 640 (the last one 260) as B arrives
+@pytest.mark.parametrize("shape", [(300, 200, 100), (5000, 700, 300), (9000, 64, 50),
+                                   (4200, 2048, 4100)])
 @pytest.mark.parametrize("pinned", [True, False])
 @pytest.mark.parametrize("alpha,beta", [(0.75, -1.25), (1.0, 0.0)])
 def test_host_entry_against_oracle(shape, pinned, alpha, beta):
@@ -40,6 +43,12 @@ def test_host_entry_against_oracle(shape, pinned, alpha, beta):
     rc = sg.sgemm_f32_host(M, N, K, alpha, bufA, K + 3, bufB, N + 1, beta, bufC, N + 5, stream)
     assert rc == 0
     stream.synchronize()
+    if M * N * K > 10**9:  # oracle on sampled rows of both blocks (block 0 ends at row 2048)
+        rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(2040, 2056),
+                                         np.random.default_rng(M).integers(0, M, 40), [M - 1]]))
+        R, S = oracle.sgemm_f64_rows(A, B, C, alpha, beta, rows)
+        assert_bound(hC.numpy()[rows], R, S, beta, C.numpy()[rows], f"host {shape} pinned={pinned}")
+        return
     R, S = oracle.sgemm_f64(A, B, C, alpha, beta)
     assert_bound(hC.numpy(), R, S, beta, C.numpy(), f"host {shape} pinned={pinned}")
     assert torch.isnan(bufC[:, N:]).all(), "padding columns of C must be untouched"
