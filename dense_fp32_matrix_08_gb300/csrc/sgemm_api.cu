@@ -63,6 +63,8 @@ struct DeviceState {
   int *status = nullptr;  // device address of g_ffma_status
   cudaMemPool_t pool = nullptr;  // split-K workspace pool of this device
   cudaError_t err = cudaSuccess;
+  // CTAs resident at once in clusters of S, per configuration (cluster_capacity_table)
+  int cluster_cap[kNumVariants * (kMaxClusterSplit + 1)] = {};
 };
 static DeviceState g_dev[kMaxDevices];
 
@@ -87,6 +89,19 @@ cudaError_t device_setup(int *num_sms) {
     if (err == cudaSuccess) err = kpair_setup();
     if (err == cudaSuccess)
       err = cudaGetSymbolAddress(reinterpret_cast<void **>(&st.status), g_ffma_status);
+    // cluster capacities of the configurations that can finish split tiles in a cluster
+    for (int v = 0; v < kNumVariants && err == cudaSuccess; ++v) {
+      if (!cluster_split_ok(v, 2)) continue;
+      KernelFn fn = nullptr;
+      for (int a = 0; a < 3 && !fn; ++a)
+        for (int b = 0; b < 3 && !fn; ++b) fn = kKernels[v].k[a][b];
+      for (int S = 2; S <= kMaxClusterSplit; ++S)
+        st.cluster_cap[v * (kMaxClusterSplit + 1) + S] =
+            kVariants[v].tma ? tma_cluster_ctas(kVariants[v].inst, S)
+            : fn != nullptr  ? cluster_ctas_of(fn, kVariants[v].threads,
+                                               (size_t)kVariants[v].smem_bytes, S)
+                             : 0;
+    }
     // A pool of the library's own for split-K workspaces. It keeps freed memory (release
     // threshold: never), so a stream-ordered allocation of a recently freed size is a
     // cheap reuse instead of a fresh mapping; the default pool returns its memory at every
@@ -175,6 +190,13 @@ static Plan automatic_plan(const Problem &pr, float alpha, float beta, int num_s
   if (tuned_lookup(pr, beta != 0.0f, num_sms, &v, &sp))
     return cached_plan(pr, alpha, beta, num_sms, v, sp);
   return cached_plan(pr, alpha, beta, num_sms, -1, 0);
+}
+
+const int *cluster_capacity_table() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_dev[dev].err == cudaSuccess && g_dev[dev].num_sms > 0 ? g_dev[dev].cluster_cap
+                                                                 : nullptr;
 }
 
 static int *status_word() {
@@ -287,6 +309,9 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   p.tiles_n = pl.tiles_n;
   p.group_m = pl.group_m;
   p.vec_c = vec_c ? 1 : 0;
+  p.cluster = pl.cluster ? 1 : 0;
+  if (pl.cluster && (!cluster_split_ok(pl.variant, pl.split) || pl.main_tiles != 0))
+    return kErrBadVariant;  // (the planner makes no such plan)
   if (vs.kpair) {
     const float *Bt = B;
     long long ldbt = pr.ldb;
@@ -350,12 +375,14 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
   const KernelFn fn = kKernels[pl.variant].k[apath][bpath];
   if (fn == nullptr) return kErrBadVariant;  // forced variant without transposed paths
   if (pl.ctas <= 0) return (int)cudaErrorInvalidConfiguration;
-  fn<<<pl.ctas, vs.threads, vs.smem_bytes, stream>>>(p);
+  cudaError_t le = launch_1d(fn, pl.ctas, vs.threads, (size_t)vs.smem_bytes,
+                             pl.cluster ? pl.split : 1, stream, p);
+  if (le != cudaSuccess) return (int)le;
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return (int)e;
   const long long tail_tiles = (long long)pl.tiles_m * pl.tiles_n - pl.main_tiles;
-  if (tail_tiles > 0) {
+  if (tail_tiles > 0 && !pl.cluster) {
     const long long work = (long long)tail_tiles * vs.BM * (vs.BN / 4);
     int rgrid = 1, rblock = 256;
     reduce_shape(work, num_sms, &rgrid, &rblock);
@@ -394,6 +421,7 @@ static int sgemm_entry(int M, int N, int K, float alpha, const float *A, int lda
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
   thin_cluster_capacity(pr.cluster_ctas);
+  pr.cluster_cap = cluster_capacity_table();
   Plan pl = (force_v < 0 && force_split == 0)
                 ? automatic_plan(pr, alpha, beta, num_sms)
                 : cached_plan(pr, alpha, beta, num_sms, force_v, force_split);
@@ -503,6 +531,7 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
     cudaError_t e = device_setup(&num_sms);
     if (e != cudaSuccess) return (int)e;
     thin_cluster_capacity(pr.cluster_ctas);
+    pr.cluster_cap = cluster_capacity_table();
   }
   Plan pl;
   if (M == 0 || N == 0) {

@@ -56,6 +56,10 @@ struct GemmParams {
   int tiles_m, tiles_n;
   int group_m;        // tile-rows per L2 group
   int vec_c;          // 1: C is 16-byte aligned with ldc % 4 == 0 (128-bit epilogue)
+  // 1: every tile is split (main_tiles == 0, split <= 8) and the grid is launched in
+  // clusters of `split` CTAs, one per slice of a tile: the slices are added through
+  // distributed shared memory (cluster_split_finish) instead of the workspace
+  int cluster;
 };
 
 // ------------------------------------------------------------------------------------
@@ -201,6 +205,89 @@ __device__ __forceinline__ float2 unpack2(unsigned long long v) {
   float2 r;
   asm("mov.b64 {%0, %1}, %2;\n" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
+}
+
+// ---- thread-block clusters (sm_90+): rank, barrier, distributed shared memory loads ----
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+
+// Every thread of every CTA of the cluster; orders shared-memory writes before it with
+// reads after it, across the cluster.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// 16 bytes of CTA `rank`'s shared memory at the offset of the local address `local`.
+__device__ __forceinline__ float4 ld_cluster4(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(local), "r"(rank));
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(remote)
+               : "memory");
+  return v;
+}
+
+// Split-K finish inside a cluster (GemmParams::cluster). Every CTA of the cluster holds its
+// K slice's BM x BN partial tile at `part` in its own shared memory, row-major, 16-byte
+// aligned (out-of-range rows and columns hold zeros). CTA rank r finishes float4 groups
+// [r * per, (r + 1) * per) of the tile: the S partials added in rank (= slice) order, then
+// C = alpha * sum + beta * C (beta == 0: C not read) with the usual masks. The call
+// synchronises the cluster before and after; every thread of every CTA must make it.
+template <int BM, int BN, int THREADS>
+__device__ __forceinline__ void cluster_split_finish(const float *part, const GemmParams &p,
+                                                     int m0, int n0) {
+  constexpr int G = BM * BN / 4;  // float4 groups of the tile
+  constexpr int QMAX = 8;         // largest cluster (portable size)
+  const int S = p.split;
+  cluster_sync_all();  // the cluster's partial tiles are complete
+  const uint32_t rank = cluster_rank();
+  const int per = (G + S - 1) / S;
+  const int e_end = min(G, ((int)rank + 1) * per);
+  const uint32_t base = (uint32_t)__cvta_generic_to_shared(part);
+  for (int e = (int)rank * per + (int)threadIdx.x; e < e_end; e += THREADS) {
+    float4 v[QMAX];
+#pragma unroll
+    for (int q = 0; q < QMAX; ++q)  // every load in flight before the adds
+      if (q < S) v[q] = ld_cluster4(base + 16u * (uint32_t)e, (uint32_t)q);
+    float4 s = v[0];
+#pragma unroll
+    for (int q = 1; q < QMAX; ++q)
+      if (q < S) {
+        s.x += v[q].x;
+        s.y += v[q].y;
+        s.z += v[q].z;
+        s.w += v[q].w;
+      }
+    const int row = m0 + e / (BN / 4);
+    const int col = n0 + (e % (BN / 4)) * 4;
+    if (row >= p.M || col >= p.N) continue;
+    const float r[4] = {s.x, s.y, s.z, s.w};
+    float *dst = p.C + (long long)row * p.ldc + col;
+    if (p.vec_c && col + 3 < p.N) {
+      float4 out;
+      if (p.beta != 0.0f) {
+        const float4 old = *reinterpret_cast<const float4 *>(dst);
+        out = make_float4(fmaf(p.alpha, r[0], p.beta * old.x), fmaf(p.alpha, r[1], p.beta * old.y),
+                          fmaf(p.alpha, r[2], p.beta * old.z), fmaf(p.alpha, r[3], p.beta * old.w));
+      } else {
+        out = make_float4(p.alpha * r[0], p.alpha * r[1], p.alpha * r[2], p.alpha * r[3]);
+      }
+      *reinterpret_cast<float4 *>(dst) = out;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (col + q < p.N)
+          dst[q] = (p.beta != 0.0f) ? fmaf(p.alpha, r[q], p.beta * dst[q]) : p.alpha * r[q];
+    }
+  }
+  cluster_sync_all();  // no CTA leaves while another may still read its partial
 }
 
 // Grouped tile order: GROUP_M tile-rows are swept column by column before moving on.
@@ -493,8 +580,11 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
   };
   if (partial) {
     // Whole partial tile, in range or not (out-of-range rows and columns hold zeros,
-    // since their loads were zero-filled); 16-byte stores, ws 16-byte aligned.
-    float *wt = p.ws + (long long)(w - p.main_tiles) * (BM * BN);
+    // since their loads were zero-filled); 16-byte stores, ws 16-byte aligned. In cluster
+    // mode the tile goes to this CTA's shared memory (the ring is free once every warp is
+    // past the K loop) and the cluster finishes it.
+    if (p.cluster) __syncthreads();
+    float *wt = p.cluster ? smem : p.ws + (long long)(w - p.main_tiles) * (BM * BN);
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
       const int r = a_row0 + (i >> 2) * LM * 4 + (i & 3);
@@ -506,6 +596,7 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
             make_float4(v[0], v[1], v[2], v[3]);
       }
     }
+    if (p.cluster) cluster_split_finish<BM, BN, Cfg::NT>(smem, p, m0, n0);
     return;
   }
   const int row_base = m0 + a_row0;

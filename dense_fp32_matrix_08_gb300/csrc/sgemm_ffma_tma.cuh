@@ -66,6 +66,7 @@ struct TmaCfg {
   static_assert(STAGES >= 2, "a ring needs two stages");
   static_assert(AMODE >= 0 && AMODE <= 2, "A read mode");
   static_assert(!TX || BM == THREADS, "transpose: one A row per thread");
+  static_assert(BM * BN * 4 <= STAGES * STAGE_BYTES, "a partial tile fits in the ring");
 };
 
 template <class Cfg>
@@ -277,14 +278,18 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
     for (int kt = issued - 1; kt >= 0 && kt >= issued - STAGES; --kt)
       mbar_wait(bars + 8 * (kt % STAGES), (uint32_t)(kt / STAGES) & 1u);
   }
-  if (!ok) return;
+  if (!ok && !p.cluster) return;  // (cluster mode: every CTA must reach the cluster barriers)
 
   // ---- epilogue: thread element (i, 4 jj + e) is row trow(i), column b_col0 + 16 jj + e
   auto trow = [&](int i) {
     return Cfg::AT ? a_col0 + (i & 3) + 32 * (i >> 2) : a_row + 8 * i;
   };
   if (partial) {
-    float *wt = p.ws + (long long)(w - p.main_tiles) * (BM * BN);
+    // cluster mode: the partial tile goes to this CTA's shared memory (the ring, free once
+    // every warp is past the K loop and the copies are drained) and the cluster finishes it
+    if (p.cluster) __syncthreads();
+    float *part = reinterpret_cast<float *>(smem_raw + (base - raw));
+    float *wt = p.cluster ? part : p.ws + (long long)(w - p.main_tiles) * (BM * BN);
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
@@ -293,6 +298,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
         *reinterpret_cast<float4 *>(wt + trow(i) * BN + b_col0 + 16 * jj) =
             make_float4(lo.x, lo.y, hi.x, hi.y);
       }
+    if (p.cluster) cluster_split_finish<BM, BN, THREADS>(part, p, m0, n0);
     return;
   }
 #pragma unroll

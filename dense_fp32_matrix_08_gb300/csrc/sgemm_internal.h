@@ -27,6 +27,27 @@ bool encode_map_2d_swizzle(CUtensorMap *map, const float *ptr, long long rows, l
 struct GemmParams;
 struct Problem;
 
+// Launch `kernel` on a 1-D grid, in thread-block clusters of `cluster` CTAs along x when
+// cluster > 1 (grid a multiple of it), else as a plain launch.
+template <class... KArgs, class... Args>
+cudaError_t launch_1d(void (*kernel)(KArgs...), int grid, int threads, size_t smem,
+                      int cluster, cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)(cluster > 1 ? cluster : 1);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = cluster > 1 ? 1 : 0;
+  if (cluster > 1 && grid % cluster != 0) return cudaErrorInvalidConfiguration;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Plan recorded by sgemm_f32_autotune for this problem (shape, flags, beta != 0) on a GPU
 // with num_sms SMs: the forced variant and split to use. False when none is recorded.
 bool tuned_lookup(const Problem &pr, bool beta_nz, int num_sms, int *variant, int *split);
@@ -57,6 +78,36 @@ void thin_cluster_capacity(int ctas[4]);
 cudaError_t tma_setup();
 cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
                        const GemmParams &p, int ctas, int *status, cudaStream_t stream);
+// CTAs of TMA-fed instance `inst` resident at once in clusters of `cluster` CTAs on the
+// current device (cudaOccupancyMaxActiveClusters; 0 if the query fails).
+int tma_cluster_ctas(int inst, int cluster);
+
+// CTAs resident at once in clusters of S (index v * (kMaxClusterSplit + 1) + S) for every
+// configuration that can finish split tiles in a cluster, on the current device; filled
+// by device_setup. Null before setup.
+const int *cluster_capacity_table();
+
+// Occupancy query for a kernel launched in 1-D clusters of `cluster` CTAs.
+template <class F>
+int cluster_ctas_of(F kernel, int threads, size_t smem, int cluster) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)cluster, 1, 1);
+  cfg.blockDim = dim3((unsigned)threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = (unsigned)cluster;
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return n * cluster;
+}
 
 // K-paired TMA-fed GEMM (sgemm_ffma_kpair.cuh): one-time kernel attributes for the current
 // device, and a launch with the given ring depth (4, 5 or 6 stages).

@@ -24,8 +24,11 @@ struct Problem {
   bool kpair_ok = false;       // op(A) = A row-major, 16-byte aligned, lda % 4 == 0
   bool b_kmajor = false;       // op(B) = B_st^T with B_st 16-byte aligned, ldb % 4 == 0
   // CTAs of the cluster thin kernel that the device holds at once in clusters of 1, 2, 4
-  // and 8 (queried from the driver; 0 = unknown, modelled by cluster_ctas_model)
+  // and 8 (queried from the driver; 0 = unknown, modelled by cluster_ctas)
   int cluster_ctas[4] = {0, 0, 0, 0};
+  // CTAs of configuration v resident at once in clusters of S, at v * 9 + S (queried from
+  // the driver; null = unknown)
+  const int *cluster_cap = nullptr;
 };
 
 // Shape of one compiled tile configuration (mirrors TileConfig in sgemm_ffma.cuh).
@@ -153,11 +156,26 @@ struct Plan {
   size_t pack_a_bytes = 0, pack_b_bytes = 0;
   // k-major TMA-fed variants: A^T (K x ldat) made by a transpose pre-pass (in pack_a_bytes)
   bool at_a = false;
+  // every tile split (main_tiles == 0) into split <= 8 slices that run as one thread-block
+  // cluster and add their partial tiles through distributed shared memory: no partial-tile
+  // workspace, no reduce launch
+  bool cluster = false;
   size_t pre_bytes = 0;
   double cycles = 0;    // modelled cost
 };
 
 inline long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+constexpr int kMaxClusterSplit = 8;  // portable cluster size
+
+// Whether a split of every tile of variant v into `split` slices can be finished inside a
+// cluster: the GEMM kernels (not the thin or K-paired ones) whose shared memory holds a
+// BM x BN FP32 tile, and 2 .. 8 slices.
+inline bool cluster_split_ok(int v, int split) {
+  const VariantShape &s = kVariants[v];
+  return !s.thin && !s.kpair && split >= 2 && split <= kMaxClusterSplit &&
+         (long long)s.BM * s.BN * 4 <= (long long)smem_of(s.BM, s.BN, s.BK, s.stages, s.mode);
+}
 
 // CTAs of the cluster thin kernel resident at once in clusters of S = 1 << l2 CTAs: the
 // driver's figure when known, else a model of a GPU whose SMs sit in GPCs of about 19 SMs
@@ -373,14 +391,28 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
     }
   }
   pl.pre_bytes = pl.bt_bytes + pl.pack_a_bytes + pl.pack_b_bytes;
+  // Clusters are placed within one GPC each, so fewer CTAs may be resident at once than
+  // `slots`: take them only when that costs no extra wave (with the driver's figure; else
+  // when a sixth of the slots to spare covers the loss).
+  long long cap = (long long)(0.85 * (double)slots);
+  if (p.cluster_cap != nullptr && split >= 2 && split <= kMaxClusterSplit)
+    cap = p.cluster_cap[v * (kMaxClusterSplit + 1) + split];
+  const bool cluster_fits = cap > 0 && ceil_div(slices, cap) <= ceil_div(slices, slots);
+  if (main == 0 && cluster_split_ok(v, split) && cluster_fits) {
+    // the cluster adds the slices in shared memory: no partial tiles in HBM and no reduce
+    // launch; two cluster barriers and each CTA reading one tile's worth over DSMEM
+    pl.cluster = true;
+    gemm_bytes -= part_bytes;
+    reduce = 1500.0 + (double)s.BM * s.BN * 4.0 / 64.0;
+  }
   pl.main_tiles = (int)main;
   pl.split = split;
   pl.k_per_split = (int)(kt_per * s.BK);
   pl.group_m = std::min(16, pl.tiles_m);
   pl.ctas = (int)(main + slices);
-  pl.launches = (slices > 0 ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0) +
+  pl.launches = (slices > 0 && !pl.cluster ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0) +
                 (pl.pack_a || pl.at_a ? 1 : 0) + (pl.pack_b ? 1 : 0);
-  pl.ws_bytes = pl.pre_bytes + (slices > 0 ? (size_t)part_bytes : 0);
+  pl.ws_bytes = pl.pre_bytes + (slices > 0 && !pl.cluster ? (size_t)part_bytes : 0);
   pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce + bt_cycles;
   if (main + slices > 0x7fffffffLL) {  // grid too large for one launch
     pl.ctas = 0;

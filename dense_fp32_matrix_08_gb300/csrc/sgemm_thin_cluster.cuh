@@ -64,29 +64,6 @@ static_assert(PART_BYTES <= SMALL_RING, "the CTA partial fits in the small ring"
 static_assert((TILE_FLOATS / 4) % MAX_CLUSTER == 0, "the tile splits over a cluster");
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
-  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
-}
-
-// 16 bytes of CTA `rank`'s shared memory at the offset of the local address `local`.
-__device__ __forceinline__ float4 ld_cluster4(uint32_t local, uint32_t rank) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(remote) : "r"(local), "r"(rank));
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];\n"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(remote)
-               : "memory");
-  return v;
-}
-
 }  // namespace cl
 
 // grid = (wide tiles, S, small tiles) launched in clusters of (1, S, 1), S = p.split; the CTA

@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(mt::THREADS, 1)
 
   const int wblk = blockIdx.x, slice = blockIdx.y, sblk = blockIdx.z;
   const int w0 = wblk * BNC, s0 = sblk * MT;
-  const int wide = TN ? p.M : p.N, small = TN ? p.N : p.M;
+  const int small = TN ? p.N : p.M;
   const int k0 = slice * p.k_per_split;
   const int KS = min(p.K - k0, p.k_per_split);  // >= 1: the host makes no empty slice
   const int NCH = (KS + KC - 1) / KC;           // chunks in the slice

@@ -42,9 +42,8 @@ cudaError_t launch(const float *A, long long lda, const float *B, long long ldb,
   if (!ok_a ||
       !encode_map_2d(&map_b, B, p.K, p.N, ldb, Cfg::BN, Cfg::BK, false))
     return cudaErrorInvalidValue;
-  tma::sgemm_tma_kernel<Cfg><<<ctas, Cfg::THREADS, Cfg::SMEM_BYTES, stream>>>(map_a, map_b, p,
-                                                                             status);
-  return cudaGetLastError();
+  return launch_1d(tma::sgemm_tma_kernel<Cfg>, ctas, Cfg::THREADS, Cfg::SMEM_BYTES,
+                   p.cluster ? p.split : 1, stream, map_a, map_b, p, status);
 }
 
 }  // namespace
@@ -68,6 +67,28 @@ cudaError_t tma_setup() {
     g_err[dev] = err;
   });
   return g_err[dev];
+}
+
+int tma_cluster_ctas(int inst, int cluster) {
+  switch (inst) {
+#define SGEMM_TMA_CLUSTER_CASE(i)                                                          \
+  case i:                                                                                  \
+    return cluster_ctas_of(tma::sgemm_tma_kernel<Tma##i>, Tma##i::THREADS, Tma##i::SMEM_BYTES, \
+                           cluster);
+    SGEMM_TMA_CLUSTER_CASE(0)
+    SGEMM_TMA_CLUSTER_CASE(1)
+    SGEMM_TMA_CLUSTER_CASE(2)
+    SGEMM_TMA_CLUSTER_CASE(3)
+    SGEMM_TMA_CLUSTER_CASE(4)
+    SGEMM_TMA_CLUSTER_CASE(5)
+    SGEMM_TMA_CLUSTER_CASE(6)
+    SGEMM_TMA_CLUSTER_CASE(7)
+    SGEMM_TMA_CLUSTER_CASE(8)
+    SGEMM_TMA_CLUSTER_CASE(9)
+#undef SGEMM_TMA_CLUSTER_CASE
+    default:
+      return 0;
+  }
 }
 
 cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,

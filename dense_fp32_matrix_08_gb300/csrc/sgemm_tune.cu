@@ -102,6 +102,7 @@ int sgemm_f32_autotune(int transa, int transb, int M, int N, int K, float alpha,
   cudaError_t e = device_setup(&num_sms);
   if (e != cudaSuccess) return (int)e;
   thin_cluster_capacity(pr.cluster_ctas);
+  pr.cluster_cap = cluster_capacity_table();
   const bool beta_nz = beta != 0.0f;
 
   // Candidates: every configuration with the model's split choice, no split, and whole

@@ -119,6 +119,14 @@ def test_plan_thin_shapes_use_thin_tiles_and_split_k():
             assert p["ws_bytes"] > 0
 
 
+def test_plan_small_cube_finishes_split_in_a_cluster():
+    """256^3 splits every tile along K: the slices run as one cluster and add their partial
+    tiles in shared memory, so the call is one launch with no workspace."""
+    p = _plan(256, 256, 256, beta=0.0)
+    assert p["split"] > 1 and p["main_tiles"] == 0
+    assert p["launches"] == 1 and p["ws_bytes"] == 0
+
+
 TMA_VARIANTS = (26, 30, 31, 32, 37, 38)  # TMA-fed, A as stored (aligned copies if needed)
 AT_VARIANTS = (35, 36, 39, 40)  # TMA-fed, reading a transposed copy of A (B copied if needed)
 
@@ -147,6 +155,10 @@ def test_plan_workspace_formula():
             pre, copies = pre + r256(4 * K * (-(-N // 4) * 4)), copies + 1
         if p["variant"] in THIN_CLUSTER:
             assert p["ws_bytes"] == 0 and p["launches"] == 1
+        elif p["split"] > 1 and p["launches"] == 1 + copies:
+            # every tile split into at most 8 slices that a thread-block cluster adds in
+            # shared memory: no partial tiles, no reduce launch
+            assert p["main_tiles"] == 0 and p["split"] <= 8 and p["ws_bytes"] == pre
         elif p["split"] > 1:
             assert split_tiles > 0 and p["launches"] == 2 + copies
             assert p["ws_bytes"] == pre + 4 * p["split"] * split_tiles * info["BM"] * info["BN"]

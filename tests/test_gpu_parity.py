@@ -216,6 +216,28 @@ def test_thin_cluster_sizes(thin_n, cluster, beta):
         assert torch.equal(out, again), (M, N, K)
 
 
+CLUSTER_SPLIT_VARIANTS = (2, 12, 32, 35, 37)  # copy-fed and TMA-fed (A as stored / k-major)
+
+
+@pytest.mark.parametrize("variant", CLUSTER_SPLIT_VARIANTS)
+@pytest.mark.parametrize("split", [2, 5, 8])
+@pytest.mark.parametrize("beta", [0.0, -1.25])
+def test_cluster_split_finish(variant, split, beta):
+    """Every tile split into 2 .. 8 K slices that run as one thread-block cluster and add
+    their partial tiles through distributed shared memory (no workspace, no reduce
+    launch): ragged tiles, K slices ending inside a K block, beta = 0 and beta != 0, and a
+    bitwise-equal second run (the slices are added in rank order)."""
+    for (M, N, K) in [(257, 255, 1000), (130, 100, 777), (1024, 1024, 1024)]:
+        A, B, C = make_inputs(M, N, K, seed=M + N + K + split)
+        lds = (-(-K // 4) * 4, -(-N // 4) * 4, None)
+        out, guard = _run(A, B, C, 0.75, beta, *lds, variant=variant, split=split)
+        assert guard, (M, N, K)
+        R, S = oracle.sgemm_f64(A, B, C, 0.75, beta)
+        assert_bound(out.numpy(), R, S, beta, C.numpy(), f"v{variant} cluster {split} {M,N,K}")
+        again, _ = _run(A, B, C, 0.75, beta, *lds, variant=variant, split=split)
+        assert torch.equal(out, again), (variant, split, M, N, K)
+
+
 # --------------------------------------------------------------------------------------
 # BLAS special cases and contract details.
 
