@@ -334,14 +334,18 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
                          (double)s.BM * s.BN * 4.0 / (3400.0 / num_sms);
   // CTAs start in index order, `slots` at a time: whole tiles first, then slices. A round
   // with fewer CTAs than slots leaves some SMs with fewer resident CTAs, which then run
-  // faster, nearly in proportion: a CTA alone on an SM that holds min_blocks takes about
-  // (1 / min_blocks)^0.85 of its shared-SM time (calibrated on 4096^3 and 8192^3).
+  // faster, though less than in proportion: n of min_blocks CTAs on an SM take about
+  // (n / min_blocks)^0.85 of their shared-SM time, and a CTA alone on its SM (4 warps,
+  // one per scheduler, too few to keep the FP32 pipe busy) (1 / min_blocks)^0.6
+  // (calibrated on 4096^3 and 8192^3, and on the last wave of 4099 x 3001 x 777).
   // Closed form (no loop over rounds): full rounds of whole tiles; one round mixing the
   // remaining whole tiles with the first slices; full rounds of slices; a last partial
   // round of slices.
   const long long slices = tail * split;
   auto partial = [&](long long n, double t) {
-    return n > 0 ? t * std::pow((double)ceil_div(n, num_sms) / s.min_blocks, 0.85) : 0.0;
+    if (n <= 0) return 0.0;
+    const long long per_sm = ceil_div(n, num_sms);
+    return t * std::pow((double)per_sm / s.min_blocks, per_sm == 1 ? 0.6 : 0.85);
   };
   double compute = (double)(main / slots) * t_full;
   const long long rem_full = main % slots;
