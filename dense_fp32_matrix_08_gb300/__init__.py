@@ -22,7 +22,7 @@ __all__ = [
     "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_status", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
     "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
-    "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm", "EXPORTED",
+    "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -34,7 +34,7 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status",
             "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
             "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load",
-            "sgemm_f32_host")
+            "sgemm_f32_host", "sgemm_f32_wait_selftest")
 
 
 class SgemmError(RuntimeError):
@@ -74,6 +74,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_3xtf32_workspace_size.argtypes = [i, i, i, psz]
     L.sgemm_f32_3xtf32_status.argtypes = [pi]
     L.sgemm_f32_status.argtypes = [pi]
+    L.sgemm_f32_wait_selftest.argtypes = [pi, ctypes.POINTER(ctypes.c_float)]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
@@ -240,6 +241,13 @@ def sgemm_f32_status() -> tuple[int, int]:
     v = ctypes.c_int(0)
     rc = lib.sgemm_f32_status(ctypes.byref(v))
     return rc, v.value
+
+
+def sgemm_f32_wait_selftest() -> dict:
+    """Run the bounded-wait self-test: {"status", "timed_out", "seconds"} (see the header)."""
+    t, sec = ctypes.c_int(0), ctypes.c_float(0.0)
+    rc = lib.sgemm_f32_wait_selftest(ctypes.byref(t), ctypes.byref(sec))
+    return {"status": rc, "timed_out": t.value, "seconds": sec.value}
 
 
 def sgemm_f32_3xtf32_status() -> tuple[int, int]:

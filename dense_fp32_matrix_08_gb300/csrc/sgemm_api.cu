@@ -17,6 +17,7 @@
 #include "sgemm_thin.cuh"
 #include "sgemm_internal.h"
 #include "sgemm_plan.h"
+#include "sgemm_ptx.cuh"
 #include "sgemm_variants.cuh"
 
 namespace sgemm {
@@ -197,6 +198,20 @@ const int *cluster_capacity_table() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   return g_dev[dev].err == cudaSuccess && g_dev[dev].num_sms > 0 ? g_dev[dev].cluster_cap
                                                                  : nullptr;
+}
+
+// One warp waits, with the kernels' own bounded wait, for a phase of an mbarrier that
+// nothing ever completes; *out = 1 when the wait gave up, as it must (sgemm_f32_wait_selftest).
+__global__ void wait_selftest_kernel(int *out) {
+  __shared__ __align__(8) unsigned long long bar;
+  const uint32_t b = saddr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    mbar_init_fence();
+  }
+  __syncwarp();
+  const bool done = mbar_wait(b, 0);  // no arrival is ever made
+  if (threadIdx.x == 0) *out = done ? 0 : 1;
 }
 
 static int *status_word() {
@@ -564,6 +579,42 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
 }
 
 const char *sgemm_f32_version(void) { return "sgemm_f32 0.1.0 sm_103a"; }
+
+int sgemm_f32_wait_selftest(int *timed_out, float *seconds) {
+  if (timed_out) *timed_out = 0;
+  if (seconds) *seconds = 0.0f;
+  int num_sms = 0;
+  cudaError_t e = device_setup(&num_sms);
+  if (e != cudaSuccess) return (int)e;
+  int *d = nullptr;
+  e = cudaMalloc(reinterpret_cast<void **>(&d), sizeof(int));
+  if (e != cudaSuccess) return (int)e;
+  cudaStream_t s = nullptr;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaEventCreate(&e0);
+  if (e == cudaSuccess) e = cudaEventCreate(&e1);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d, 0, sizeof(int), s);
+  if (e == cudaSuccess) e = cudaEventRecord(e0, s);
+  if (e == cudaSuccess) {
+    wait_selftest_kernel<<<1, 32, 0, s>>>(d);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(e1, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  int v = 0;
+  float ms = 0.0f;
+  if (e == cudaSuccess) e = cudaMemcpy(&v, d, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, e0, e1);
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  if (s) cudaStreamDestroy(s);
+  cudaFree(d);
+  if (e != cudaSuccess) return (int)e;
+  if (timed_out) *timed_out = v;
+  if (seconds) *seconds = ms / 1000.0f;
+  return 0;
+}
 
 int sgemm_f32_status(int *status) {
   int v = 0;

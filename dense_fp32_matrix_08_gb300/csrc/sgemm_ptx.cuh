@@ -1,5 +1,6 @@
 // PTX wrappers shared by the TMA-fed kernels: mbarriers and 2-D tensor copies (sm_90+
-// features, compiled here for sm_103a). Every wait is bounded by a poll limit.
+// features, compiled here for sm_103a). Every wait is bounded in time: after about one
+// second without the awaited phase it gives up and the kernel reports it.
 #pragma once
 
 #include <cuda.h>
@@ -8,7 +9,13 @@
 
 namespace sgemm {
 
-constexpr uint32_t kSpinLimit = 1u << 26;  // try_wait polls before a wait gives up
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // a wait gives up after 1 s
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t saddr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -46,10 +53,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return done != 0;
 }
 
-// Wait for the phase of parity `parity` to complete; false if the poll limit runs out.
+// Wait for the phase of parity `parity` to complete; false if it has not completed after
+// kWaitLimitNs of the global timer (or, should the timer not advance, 2^27 polls). The
+// first poll is the whole cost when the phase is already done.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t round = 0; round < (1u << 22); ++round) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
   return false;
 }
 

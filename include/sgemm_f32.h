@@ -267,8 +267,17 @@ int sgemm_f32_3xtf32_status(int *status);
 /* Reads and clears the device status word of the TMA-fed FFMA kernel (synchronising copy
  * on the legacy stream): 0 = fine; 1 or 2 = a bounded mbarrier wait gave up (a consumer
  * waiting for data, or the producer waiting for a free stage), in which case the kernel
- * stopped computing and the result of that call is not valid. */
+ * stopped computing and the result of that call is not valid. Every mbarrier wait in the
+ * library's kernels gives up after about one second of the GPU's global timer. */
 int sgemm_f32_status(int *status);
+
+/* Failure-path self-test of that bounded wait: one warp waits, with the kernels' own wait,
+ * for a phase of an mbarrier that nothing ever completes. The wait must give up after
+ * about one second and the kernel must end normally. Outputs: *timed_out = 1 if the wait
+ * gave up (0 would mean it saw a phase complete), *seconds = the kernel's duration (CUDA
+ * events). Synchronous (own stream); the context stays usable afterwards. Returns 0 or a
+ * cudaError_t. */
+int sgemm_f32_wait_selftest(int *timed_out, float *seconds);
 
 /* C = alpha * A * B + beta * C with A, B and C in HOST memory (row-major, the ld rules of
  * sgemm_f32). The product runs on the GPU in row blocks of about 2048 rows: B is copied to
