@@ -38,23 +38,42 @@ __global__ void scale_c_kernel(float *__restrict__ C, long long ldc, int M, int 
 
 // dst (rows x ldd floats, ldd % 4 == 0, 16-byte aligned) = src (rows x cols, row stride
 // ld, any alignment): the aligned copy that lets the TMA-fed kernel read an operand whose
-// leading dimension or address TMA cannot take. Each thread copies one 4-column group of a
-// row (scalar reads, one 128-bit write); a row's last group is zero-padded up to ldd.
+// leading dimension or address TMA cannot take. A thread copies 4-column groups of a row
+// (scalar reads, one 128-bit write each), four groups per round with all 16 reads issued
+// before the writes, so that enough bytes are in flight to run at HBM speed; a row's last
+// group is zero-padded up to ldd.
 __global__ void pack_rows_kernel(const float *__restrict__ src, long long ld, int rows,
                                  int cols, float *__restrict__ dst, long long ldd) {
+  constexpr int U = 4;
   const long long quads = (cols + 3) / 4;
   const long long total = (long long)rows * quads;
-  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
-       g += (long long)gridDim.x * blockDim.x) {
-    const long long r = g / quads;
-    const int c = (int)(g - r * quads) * 4;
-    const float *s = src + r * ld + c;
-    float4 v;
-    v.x = s[0];
-    v.y = c + 1 < cols ? s[1] : 0.0f;
-    v.z = c + 2 < cols ? s[2] : 0.0f;
-    v.w = c + 3 < cols ? s[3] : 0.0f;
-    *reinterpret_cast<float4 *>(dst + r * ldd + c) = v;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; g0 < total;
+       g0 += U * stride) {
+    float4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long g = g0 + u * stride;
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (g < total) {
+        const long long r = g / quads;
+        const int c = (int)(g - r * quads) * 4;
+        const float *s = src + r * ld + c;
+        v[u].x = s[0];
+        v[u].y = c + 1 < cols ? s[1] : 0.0f;
+        v[u].z = c + 2 < cols ? s[2] : 0.0f;
+        v[u].w = c + 3 < cols ? s[3] : 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long g = g0 + u * stride;
+      if (g < total) {
+        const long long r = g / quads;
+        const int c = (int)(g - r * quads) * 4;
+        *reinterpret_cast<float4 *>(dst + r * ldd + c) = v[u];
+      }
+    }
   }
 }
 
