@@ -115,8 +115,13 @@ int sgemm_f32_autotune(int transa, int transb, int M, int N, int K, float alpha,
   std::vector<Cand> cands;
   double best_model = std::numeric_limits<double>::infinity();
   for (int v = 0; v < kNumVariants; ++v)
-    for (int s : {0, 1, -1, 2, 4, 8}) {
-      if (s > 1 && kVariants[v].thin < 5) continue;  // cluster sizes of the cluster kernels
+    for (int s : {0, 1, -1, 2, 3, 4, 6, 8, -2, -3, -4, -6, -8}) {
+      // the thin kernels take the model's split, none, whole waves plus a split tail, and
+      // (the cluster thin kernels) cluster sizes 2, 4 and 8; the tile kernels every tile
+      // split 2 .. 8 ways (in a cluster where it fits) and split tails of 2 .. 8 slices
+      const int thin = kVariants[v].thin;
+      if (thin && thin < 5 && (s > 1 || s < -1)) continue;
+      if (thin >= 5 && (s < -1 || s == 3 || s == 6)) continue;
       const Plan pl = make_plan(pr, alpha, beta, num_sms, v, s);
       if (pl.variant < 0 || !(pl.cycles < std::numeric_limits<double>::infinity())) continue;
       bool dup = false;

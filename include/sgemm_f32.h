@@ -303,8 +303,11 @@ int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, int lda, co
  *
  * sgemm_f32_autotune times, on `stream` and the caller's operands, every compiled tile
  * configuration that can run op(A) op(B) for these transpose flags, shape, leading
- * dimensions and alignments. Each is timed with three split-K layouts: the model's own
- * choice, no split, and whole waves plus a split last wave. Each candidate runs once to
+ * dimensions and alignments. Each is timed with several split-K layouts: the model's own
+ * choice, no split, every tile split 2, 3, 4, 6 or 8 ways, and whole waves plus a last
+ * wave split the automatic number of ways or 2, 3, 4, 6 or 8 (the thin kernels: the
+ * model's choice, no split, a split last wave and, for the cluster thin kernels, clusters
+ * of 2, 4 and 8). Layouts that come out the same are timed once. Each candidate runs once to
  * warm up, then `reps` times (3 if reps <= 0), timed with CUDA events. Layouts the cost
  * model rates at more than 4x its best are skipped. The fastest candidate is recorded in
  * a per-process table. From then on sgemm_f32, sgemm_f32_ex, sgemm_f32_ws,
