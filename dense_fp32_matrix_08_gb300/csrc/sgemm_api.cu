@@ -45,10 +45,11 @@ static const VariantKernels kKernels[kNumVariants] = {
     VariantKernels{},
     VariantKernels{},  // cluster thin-M and thin-N kernels (sgemm_thin.cu)
     VariantKernels{},
+    VariantKernels{},  // TMA-fed 128 x 64 transposing A in the CTA (sgemm_tma.cu)
 };
 static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 33 &&
                   kThinNVariant == 34 && kThinTmaVariant == 41 &&
-                  kThinClusterVariant == 43 && kNumVariants == 45,
+                  kThinClusterVariant == 43 && kNumVariants == 46,
               "the generic variants come first, then the TMA-fed and streaming ones");
 
 // Device status word of the TMA-fed kernel (0 = fine; nonzero = a bounded wait gave up).

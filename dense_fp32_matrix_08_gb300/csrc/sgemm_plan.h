@@ -107,9 +107,11 @@ constexpr VariantShape kVariants[] = {
     // to fit 2 CTAs/SM
     {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1) + 16384, 1.028, true, false, true, false, 6},
     {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1) + 16384, 1.03, true, false, true, false, 7},
-    // 39, 40: k-major A, 128 x 64 at 4 CTAs/SM and 128 x 128 with 2 stages
-    {128, 64, 32, 128, 8, 8, 2, 4, 1, smem_of(128, 64, 32, 2, 1), 1.055, false, false, true, false, 8, 0, true},
-    {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1), 1.0, false, false, true, false, 9, 0, true},
+    // 39, 40: k-major A, 128 x 64 at 4 CTAs/SM and 128 x 128 with 2 stages. 39 is automatic
+    // with its efficiency calibrated against 35 (1.8% slower at 8192^3, 13% faster at 3000^3,
+    // 6% at 2048^3, where its 608 slots round the waves better)
+    {128, 64, 32, 128, 8, 8, 2, 4, 1, smem_of(128, 64, 32, 2, 1), 1.04, true, false, true, false, 8, 0, true, 45},
+    {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1), 1.0, false, false, true, false, 9, 0, true, 38},
     // 41: TMA-fed thin-M, 16 x 256 C tiles, 8 warps each streaming its own 8-k chunks of B
     // through 2 private stages, K slices reduced by the split-K finish (1 CTA/SM)
     {16, 256, 8, 256, 16, 8, 2, 1, 1, 0, 0.7, true, false, false, false, 0, 3},
@@ -122,6 +124,9 @@ constexpr VariantShape kVariants[] = {
     // distributed shared memory (no workspace, one launch)
     {16, 128, 8, 256, 16, 4, 4, 1, 1, 0, 0.8, true, false, false, false, 0, 5},
     {128, 16, 8, 256, 4, 16, 4, 1, 1, 0, 0.8, true, false, false, false, 0, 6},
+    // 45: 39's twin, transposing each A tile in shared memory (3 CTAs/SM; forced-only, and
+    // the substitute for 39 when a caller workspace cannot hold the A^T copy)
+    {128, 64, 32, 128, 8, 8, 2, 3, 1, smem_of(128, 64, 32, 2, 1) + 16384, 0.98, false, false, true, false, 10},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 constexpr int kTmaVariant = 26;

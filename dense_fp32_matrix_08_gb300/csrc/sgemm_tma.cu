@@ -20,7 +20,8 @@ using Tma6 = tma::TmaCfg<96, 12, 2, 3, false, 2>;   // Tma1, A transposed in the
 using Tma7 = tma::TmaCfg<128, 16, 2, 2, false, 2>;  // 128 x 128, 2 stages, A transposed
 using Tma8 = tma::TmaCfg<64, 8, 2, 4, false, 1>;    // 128 x 64 on k-major A, 4 CTAs/SM
 using Tma9 = tma::TmaCfg<128, 16, 2, 2, false, 1>;  // 128 x 128 on k-major A, 2 stages
-constexpr int kInstances = 10;
+using Tma10 = tma::TmaCfg<64, 8, 2, 3, false, 2>;   // Tma8, A transposed in the CTA
+constexpr int kInstances = 11;
 
 std::once_flag g_once[64];
 cudaError_t g_err[64];
@@ -64,6 +65,7 @@ cudaError_t tma_setup() {
     if (err == cudaSuccess) err = set_smem<Tma7>();
     if (err == cudaSuccess) err = set_smem<Tma8>();
     if (err == cudaSuccess) err = set_smem<Tma9>();
+    if (err == cudaSuccess) err = set_smem<Tma10>();
     g_err[dev] = err;
   });
   return g_err[dev];
@@ -85,6 +87,7 @@ int tma_cluster_ctas(int inst, int cluster) {
     SGEMM_TMA_CLUSTER_CASE(7)
     SGEMM_TMA_CLUSTER_CASE(8)
     SGEMM_TMA_CLUSTER_CASE(9)
+    SGEMM_TMA_CLUSTER_CASE(10)
 #undef SGEMM_TMA_CLUSTER_CASE
     default:
       return 0;
@@ -93,7 +96,7 @@ int tma_cluster_ctas(int inst, int cluster) {
 
 cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, long long ldb,
                        const GemmParams &p, int ctas, int *status, cudaStream_t stream) {
-  static_assert(kInstances == 10, "instance table");
+  static_assert(kInstances == 11, "instance table");
   switch (inst) {
     case 0: return launch<Tma0>(A, lda, B, ldb, p, ctas, status, stream);
     case 1: return launch<Tma1>(A, lda, B, ldb, p, ctas, status, stream);
@@ -105,6 +108,7 @@ cudaError_t launch_tma(int inst, const float *A, long long lda, const float *B, 
     case 7: return launch<Tma7>(A, lda, B, ldb, p, ctas, status, stream);
     case 8: return launch<Tma8>(A, lda, B, ldb, p, ctas, status, stream);
     case 9: return launch<Tma9>(A, lda, B, ldb, p, ctas, status, stream);
+    case 10: return launch<Tma10>(A, lda, B, ldb, p, ctas, status, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -127,7 +127,7 @@ def test_plan_small_cube_finishes_split_in_a_cluster():
     assert p["launches"] == 1 and p["ws_bytes"] == 0
 
 
-TMA_VARIANTS = (26, 30, 31, 32, 37, 38)  # TMA-fed, A as stored (aligned copies if needed)
+TMA_VARIANTS = (26, 30, 31, 32, 37, 38, 45)  # TMA-fed, A as stored (aligned copies if needed)
 AT_VARIANTS = (35, 36, 39, 40)  # TMA-fed, reading a transposed copy of A (B copied if needed)
 
 

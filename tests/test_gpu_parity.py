@@ -15,8 +15,8 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 45  # compiled tile configurations; checked against the library below
-TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40)  # every TMA-fed instance
+NUM_VARIANTS = 46  # compiled tile configurations; checked against the library below
+TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40, 45)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
 THIN_M_TMA = 41  # TMA-fed thin-M: B must be TMA-addressable
@@ -335,9 +335,26 @@ def test_deterministic_and_ws_entry_match():
     torch.cuda.synchronize()
     assert torch.equal(dC.cpu(), o1)
     if nbytes:
+        # one byte short: refused (-13), unless the plan's only workspace is an A^T copy
+        # that the twin configuration (A transposed in shared memory) does without, in
+        # which case the result is bitwise the same
         dC2, _ = to_device_view(C)
-        assert sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, dC2, N, ws.data_ptr(),
-                               nbytes - 1) == -13
+        rc = sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, dC2, N, ws.data_ptr(), nbytes - 1)
+        assert rc in (0, -13)
+        if rc == 0:
+            torch.cuda.synchronize()
+            assert torch.equal(dC2.cpu(), o1)
+    # a plan whose split-K partial tiles need the workspace is refused when it is too small
+    M, N, K = 2100, 2600, 300
+    p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, 1.0, 0)
+    if p["split"] > 1 and p["ws_bytes"] > 0:
+        A, B, C = make_inputs(M, N, K, seed=9)
+        dA, _ = to_device_view(A)
+        dB, _ = to_device_view(B)
+        dC, _ = to_device_view(C)
+        ws = torch.empty(p["ws_bytes"], dtype=torch.uint8, device="cuda")
+        assert sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, dC, N, ws.data_ptr(),
+                               p["ws_bytes"] - 1) == -13
 
 
 def test_illegal_arguments_launch_nothing():
