@@ -163,47 +163,96 @@ __device__ __forceinline__ float tf32_rna(float x) {
 __global__ void split_rows_kernel(const float *__restrict__ X, long long ldx, int R, int Cc,
                                   float *__restrict__ hi, float *__restrict__ lo, int R_pad,
                                   int C_pad) {
+  constexpr int U = 4;  // 4-column groups per thread and round, all reads issued first
   const long long quads = C_pad / 4;
   const long long total = (long long)R_pad * quads;
-  for (long long g = blockIdx.x * (long long)blockDim.x + threadIdx.x; g < total;
-       g += (long long)gridDim.x * blockDim.x) {
-    const long long r = g / quads;
-    const int c = (int)(g - r * quads) * 4;
-    float h[4], l[4];
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long g0 = blockIdx.x * (long long)blockDim.x + threadIdx.x; g0 < total;
+       g0 += U * stride) {
+    float x[U][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x = (r < R && c + e < Cc) ? X[r * ldx + c + e] : 0.0f;
-      h[e] = tf32_rna(x);
-      l[e] = tf32_rna(x - h[e]);
+    for (int u = 0; u < U; ++u) {
+      const long long g = g0 + u * stride;
+      const long long r = g / quads;
+      const int c = (int)(g - r * quads) * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        x[u][e] = (g < total && r < R && c + e < Cc) ? X[r * ldx + c + e] : 0.0f;
     }
-    *reinterpret_cast<float4 *>(hi + r * C_pad + c) = make_float4(h[0], h[1], h[2], h[3]);
-    *reinterpret_cast<float4 *>(lo + r * C_pad + c) = make_float4(l[0], l[1], l[2], l[3]);
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const long long g = g0 + u * stride;
+      if (g >= total) break;
+      const long long r = g / quads;
+      const int c = (int)(g - r * quads) * 4;
+      float h[4], l[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        h[e] = tf32_rna(x[u][e]);
+        l[e] = tf32_rna(x[u][e] - h[e]);
+      }
+      *reinterpret_cast<float4 *>(hi + r * C_pad + c) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4 *>(lo + r * C_pad + c) = make_float4(l[0], l[1], l[2], l[3]);
+    }
   }
 }
 
 // Transposing split: out[n][k] = split(X[k][n]); X: R (=K) x Cc (=N) with ld ldx;
-// hi, lo: Cc_pad x R_pad row-major (ld = R_pad). 32 x 32 tiles through shared memory.
-__global__ void split_cols_kernel(const float *__restrict__ X, long long ldx, int R, int Cc,
-                                  float *__restrict__ hi, float *__restrict__ lo, int R_pad,
-                                  int Cc_pad) {
-  __shared__ float t[32][33];
-  const int k0 = blockIdx.y * 32, n0 = blockIdx.x * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;  // 32 x 8 threads
+// hi, lo: Cc_pad x R_pad row-major (ld = R_pad, a multiple of 4: 128-bit stores), zero
+// beyond R and Cc. 64 x 64 tiles through shared memory, grid-stride; each of the 256
+// threads has its 16 reads of a tile in flight at once (128-bit when VEC: ldx % 4 == 0 and
+// X 16-byte aligned).
+template <bool VEC>
+__global__ void __launch_bounds__(256) split_cols_kernel(const float *__restrict__ X,
+                                                         long long ldx, int R, int Cc,
+                                                         float *__restrict__ hi,
+                                                         float *__restrict__ lo, int R_pad,
+                                                         int Cc_pad) {
+  __shared__ float t[64][65];
+  const long long tiles_n = (Cc_pad + 63) / 64;
+  const long long tiles = tiles_n * ((R_pad + 63) / 64);
+  const int tid = threadIdx.x, cg = tid & 15, ro = tid >> 4;
+  for (long long tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    const int k0 = (int)(tile / tiles_n) * 64;
+    const int n0 = (int)(tile % tiles_n) * 64;
+    float v[4][4];
 #pragma unroll
-  for (int i = ty; i < 32; i += 8) {
-    const int k = k0 + i, n = n0 + tx;
-    t[i][tx] = (k < R && n < Cc) ? X[(long long)k * ldx + n] : 0.0f;
-  }
-  __syncthreads();
+    for (int i = 0; i < 4; ++i) {
+      const int k = k0 + ro + 16 * i, n = n0 + 4 * cg;
+      const float *src = X + (long long)k * ldx + n;
+      if (VEC && k < R && n + 3 < Cc) {
+        const float4 f = __ldcs(reinterpret_cast<const float4 *>(src));
+        v[i][0] = f.x;
+        v[i][1] = f.y;
+        v[i][2] = f.z;
+        v[i][3] = f.w;
+      } else {
 #pragma unroll
-  for (int i = ty; i < 32; i += 8) {
-    const int n = n0 + i, k = k0 + tx;
-    if (n < Cc_pad && k < R_pad) {
-      const float x = t[tx][i];
-      const float h = tf32_rna(x);
-      hi[(long long)n * R_pad + k] = h;
-      lo[(long long)n * R_pad + k] = tf32_rna(x - h);
+        for (int j = 0; j < 4; ++j) v[i][j] = (k < R && n + j < Cc) ? src[j] : 0.0f;
+      }
     }
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) t[ro + 16 * i][4 * cg + j] = v[i][j];
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int nl = ro + 16 * i, kl = 4 * cg;
+      const int n = n0 + nl, k = k0 + kl;
+      if (n >= Cc_pad || k >= R_pad) continue;  // R_pad is a multiple of 4: whole groups
+      float h[4], l[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float x = t[kl + j][nl];
+        h[j] = tf32_rna(x);
+        l[j] = tf32_rna(x - h[j]);
+      }
+      const long long o = (long long)n * R_pad + k;
+      *reinterpret_cast<float4 *>(hi + o) = make_float4(h[0], h[1], h[2], h[3]);
+      *reinterpret_cast<float4 *>(lo + o) = make_float4(l[0], l[1], l[2], l[3]);
+    }
+    __syncthreads();
   }
 }
 
@@ -498,9 +547,14 @@ extern "C" int sgemm_f32_3xtf32(int M, int N, int K, float alpha, const float *A
                                                       (int)sh.Kp);
   }
   {
-    dim3 grid((unsigned)(sh.Np / 32), (unsigned)(sh.Kp / 32));
-    tc::split_cols_kernel<<<grid, dim3(32, 8), 0, stream>>>(B, ldb, K, N, bh, bl, (int)sh.Kp,
-                                                            (int)sh.Np);
+    const long long tiles = ((sh.Np + 63) / 64) * ((sh.Kp + 63) / 64);
+    const int blocks = (int)std::max<long long>(1, std::min<long long>(tiles, (long long)num_sms * 8));
+    if (ldb % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0)
+      tc::split_cols_kernel<true><<<blocks, 256, 0, stream>>>(B, ldb, K, N, bh, bl, (int)sh.Kp,
+                                                              (int)sh.Np);
+    else
+      tc::split_cols_kernel<false><<<blocks, 256, 0, stream>>>(B, ldb, K, N, bh, bl,
+                                                               (int)sh.Kp, (int)sh.Np);
   }
   e = cudaGetLastError();
   if (e == cudaSuccess) {
