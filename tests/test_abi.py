@@ -127,6 +127,17 @@ def test_plan_small_cube_finishes_split_in_a_cluster():
     assert p["launches"] == 1 and p["ws_bytes"] == 0
 
 
+def test_plan_calibration_points():
+    """The model's choices at the shapes it was calibrated on (measured on GB300): 128 x 96
+    k-major tiles for the large shapes, with a split last wave at 4099 x 3001 x 777;
+    128 x 64 k-major tiles at 3000^3, where 4 CTAs per SM round the waves better."""
+    assert _plan(8192, 8192, 8192)["variant"] == 35
+    assert _plan(4096, 4096, 4096)["variant"] == 35
+    p = _plan(4099, 3001, 777)
+    assert p["variant"] == 35 and p["split"] > 1 and p["main_tiles"] > 0
+    assert _plan(3000, 3000, 3000)["variant"] == 39
+
+
 TMA_VARIANTS = (26, 30, 31, 32, 37, 38, 45)  # TMA-fed, A as stored (aligned copies if needed)
 AT_VARIANTS = (35, 36, 39, 40)  # TMA-fed, reading a transposed copy of A (B copied if needed)
 
