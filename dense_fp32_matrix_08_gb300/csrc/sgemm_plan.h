@@ -118,12 +118,12 @@ constexpr VariantShape kVariants[] = {
     // 42: TMA-fed thin-N (C^T = B^T A^T on the same kernel): 256 x 16 C tiles, A streamed
     // as [256 m][8 k] chunks
     {256, 16, 8, 256, 8, 16, 2, 1, 1, 0, 0.7, true, false, false, false, 0, 4},
-    // 43, 44: cluster thin-M / thin-N: 16 x 128 (128 x 16) C tiles, 8 warps streaming both
+    // 43, 44: cluster thin-M / thin-N: 16 x 128 (128 x 16) C tiles, 16 warps streaming both
     // operands by TMA in 8-k chunks (16 x 4 outputs per lane, every warp over the whole
     // tile), the K slices of a tile one cluster of 1, 2, 4 or 8 CTAs reduced through
     // distributed shared memory (no workspace, one launch)
-    {16, 128, 8, 256, 16, 4, 4, 1, 1, 0, 0.8, true, false, false, false, 0, 5},
-    {128, 16, 8, 256, 4, 16, 4, 1, 1, 0, 0.8, true, false, false, false, 0, 6},
+    {16, 128, 8, 512, 16, 4, 2, 1, 1, 0, 0.8, true, false, false, false, 0, 5},
+    {128, 16, 8, 512, 4, 16, 2, 1, 1, 0, 0.8, true, false, false, false, 0, 6},
     // 45: 39's twin, transposing each A tile in shared memory (3 CTAs/SM; forced-only, and
     // the substitute for 39 when a caller workspace cannot hold the A^T copy)
     {128, 64, 32, 128, 8, 8, 2, 3, 1, smem_of(128, 64, 32, 2, 1) + 16384, 0.98, false, false, true, false, 10},

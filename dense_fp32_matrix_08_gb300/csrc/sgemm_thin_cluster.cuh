@@ -10,16 +10,17 @@
 //    CTA's 128 wide indices (4 KB) plus the same 8 k of the thin ("small") operand for its 16
 //    indices (512 B). No staging prologue holds back the first FMA.
 //  * The K slices of one C tile are the CTAs of one cluster (1 x S x 1, S = 1, 2, 4 or 8).
-//    Each CTA adds its 8 warps' partial tiles in warp order, then the cluster adds the S
+//    Each CTA adds its 16 warps' partial tiles in warp order, then the cluster adds the S
 //    CTA partials through distributed shared memory in rank order, each CTA finishing 1/S
 //    of the tile with the alpha / beta epilogue. No workspace, no second launch; every
 //    output is a fixed-order sum.
 //  * The tile is 16 x 128 so that clusters of 4 fill the GPU on 16 x 4096 and 4096 x 16
 //    products (32 tiles x 4 slices = 128 CTAs, one per SM).
 //
-// Warps: 8, each with four private ring stages and the chunks c = w, w + 8, ... of the CTA's
-// K slice (lane 0 issues, the warp waits on the stage's mbarrier with a bounded poll,
-// computes, and refills the stage four chunks ahead). A lane owns all 16 small indices times
+// Warps: 16, each with two private ring stages and the chunks c = w, w + 16, ... of the
+// CTA's K slice (lane 0 issues, the warp waits on the stage's mbarrier with a bounded poll,
+// computes, and refills the stage two chunks ahead). 16 warps of two stages measured 2-7%
+// faster than 8 or 12 warps with the same bytes in flight. A lane owns all 16 small indices times
 // 4 wide indices. FFMA2 pairs run along the small dimension, {s_2p, s_2p+1} straight from
 // a 128-bit broadcast load of the small operand's k row, times the wide value duplicated
 // into both halves, {w, w}: 32 FFMA2 per k against 4 duplications and 5 shared loads. On
@@ -44,8 +45,8 @@ namespace cl {
 constexpr int MT = 16;             // small extent of a tile
 constexpr int BW = 128;            // wide extent of a tile
 constexpr int KC = 8;              // k per chunk (one pair of TMA copies)
-constexpr int WARPS = 8;
-constexpr int SPW = 4;             // private ring stages per warp
+constexpr int WARPS = 16;
+constexpr int SPW = 2;             // private ring stages per warp
 constexpr int THREADS = WARPS * 32;
 constexpr int STAGES = WARPS * SPW;
 constexpr int BIG_BYTES = KC * BW * 4;      // wide-operand part of a chunk

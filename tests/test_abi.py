@@ -82,10 +82,11 @@ def test_variant_table():
         assert info["TM"] * info["TN"] >= 16 and info["threads"] % 32 == 0
         # the CTA tile is exactly covered by its threads' accumulator tiles, once, or once
         # per k-group where several thread groups split the CTA's K range (thin-M: 4 groups,
-        # or 8 warps that each take 4 of every stage's 32 k rows, or every 8th 8-k chunk)
+        # or 8 warps that each take 4 of every stage's 32 k rows, or 16 warps that each take
+        # every 16th 8-k chunk)
         covered = info["threads"] * info["TM"] * info["TN"]
         assert covered % (info["BM"] * info["BN"]) == 0
-        assert covered // (info["BM"] * info["BN"]) in (1, 4, 8)
+        assert covered // (info["BM"] * info["BN"]) in (1, 4, 8, 16)
     assert sg.sgemm_f32_variant_info(n) is None
     big = sg.sgemm_f32_variant_info(0)
     assert big["TM"] * big["TN"] >= 64  # at least an 8x8 register outer product
