@@ -145,6 +145,23 @@ def test_whole_waves_plus_split_tail(variant, split):
     assert_bound(out.numpy(), R, S, 0.5, C.numpy(), f"v{variant} tail split {split}")
 
 
+def test_mid_size_sweep_auto_plan():
+    """Random mid-size shapes under the automatic plan, which there chooses among the
+    128 x 96 and 128 x 64 k-major tiles, cluster-finished splits and split tails. Checked
+    on sampled rows (the first and last rows, rows at tile edges, random rows) against the
+    oracle; guard bands must stay intact."""
+    rng = np.random.default_rng(11)
+    for t in range(12):
+        M, N, K = (int(rng.integers(200, 3000)) for _ in range(3))
+        A, B, C = make_inputs(M, N, K, seed=300 + t)
+        out, guard = _run(A, B, C, 1.25, -0.5)
+        assert guard, (M, N, K)
+        rows = np.unique(np.concatenate([[0, 1, M - 1], np.arange(127, M, 128)[:4],
+                                         rng.integers(0, M, 12)]))
+        R, S = oracle.sgemm_f64_rows(A, B, C, 1.25, -0.5, rows)
+        assert_bound(out.numpy()[rows], R, S, -0.5, C.numpy()[rows], f"auto {M,N,K}")
+
+
 def test_ragged_sweep_auto_plan():
     """Small M, N, K around tile edges under the automatic plan."""
     edges = [1, 2, 3, 5, 8, 15, 16, 17, 127, 128, 129, 255, 256, 257]
