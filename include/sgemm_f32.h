@@ -147,10 +147,14 @@ int sgemm_f32_ws(int M, int N, int K, float alpha, const float *A, int lda, cons
  *   variant  tile configuration index (0 .. sgemm_f32_num_variants() - 1), -1 when no
  *            GEMM kernel runs (empty problem or beta-scale only)
  *   split      K slices of each split tile (1 = no split-K)
- *   main_tiles tiles computed whole; the remaining tiles are split into `split` K slices
- *              and finished by a second, reducing kernel
- *   launches   kernels enqueued by one sgemm_f32 call
- *   ws_bytes   split-K workspace bytes
+ *   main_tiles tiles computed whole; the remaining tiles are split into `split` K slices.
+ *              These are finished by a second, reducing kernel from the workspace. When
+ *              every tile is split (main_tiles == 0) into at most 8 slices and the slices
+ *              fit as thread-block clusters, they are instead added inside the cluster
+ *              through distributed shared memory (no second kernel, no workspace)
+ *   launches   kernels enqueued by one sgemm_f32 call (pre-pass copies included)
+ *   ws_bytes   workspace bytes: pre-pass copies (A^T for the k-major configurations,
+ *              aligned copies of operands TMA cannot address) and split-K partial tiles
  * Returns the same negative codes as sgemm_f32 for illegal arguments, else 0. */
 int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta,
                    int num_sms, int *variant, int *split, int *main_tiles, int *launches,
@@ -167,12 +171,18 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
 /* sgemm_f32 with the plan forced, for tests and tuning sweeps; results satisfy the same
  * contract as sgemm_f32. `variant` in [0, sgemm_f32_num_variants()) pins the tile
  * configuration (-1: automatic). `split` >= 1 splits every tile into that many K slices
- * (1: no split-K); -1 computes the full waves of tiles whole and splits only the tiles of
- * the last, partial wave (slice count chosen to fill it); <= -2 does the same with
- * -split slices; 0 is automatic. Slice counts are clamped so that every slice holds at
- * least one K tile. Returns -14 for an out-of-range variant, for the TMA-fed
- * configuration when A or B is not 16-byte aligned with lda, ldb multiples of 4, and for
- * the K-paired configurations when A is not. */
+ * (1: no split-K; 2 .. 8 run as thread-block clusters where the configuration and the
+ * device's cluster occupancy allow, see sgemm_f32_plan); -1 computes the full waves of
+ * tiles whole and splits only the tiles of the last, partial wave (slice count chosen to
+ * fill it); <= -2 does the same with -split slices; 0 is automatic. Slice counts are
+ * clamped so that every slice holds at least one K tile. The cluster thin kernels take
+ * `split` as their cluster size, rounded up to 1, 2, 4 or 8. A TMA-fed configuration on
+ * an operand TMA cannot address (lda or ldb not a multiple of 4, or a pointer not 16-byte
+ * aligned) first copies it to aligned rows in the workspace. Returns -14 for an
+ * out-of-range variant, for a configuration that cannot run the problem (a TMA-fed one on
+ * transposed operands, see sgemm_f32_ex_forced; a thin one on a thin operand TMA cannot
+ * address), and for the K-paired configurations when A is not 16-byte aligned with lda a
+ * multiple of 4. */
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);
@@ -187,8 +197,8 @@ int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
  * -14 also when the forced configuration has no path for these transpose flags or this
  * alignment:
  *   - the TMA-fed configurations need transb = 0, and transa = 0, except the k-major ones
- *     (sgemm_f32_variant_info: 35, 36), which also take transa = 1 with A_st 16-byte
- *     aligned and lda a multiple of 4 (A_st is then read directly);
+ *     (35, 36, 39, 40), which also take transa = 1 with A_st 16-byte aligned and lda a
+ *     multiple of 4 (A_st is then read directly);
  *   - the K-paired ones need transa = 0 and A 16-byte aligned with lda a multiple of 4;
  *   - the copy-fed ones carry transposed-operand paths only in configurations 2, 3, 4, 16. */
 int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha,
