@@ -180,9 +180,9 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
  * an operand TMA cannot address (lda or ldb not a multiple of 4, or a pointer not 16-byte
  * aligned) first copies it to aligned rows in the workspace. Returns -14 for an
  * out-of-range variant, for a configuration that cannot run the problem (a TMA-fed one on
- * transposed operands, see sgemm_f32_ex_forced; a thin one on a thin operand TMA cannot
- * address), and for the K-paired configurations when A is not 16-byte aligned with lda a
- * multiple of 4. */
+ * transposed operands, see sgemm_f32_ex_forced; a TMA-fed thin one on an operand it reads
+ * by TMA that TMA cannot address), and for the K-paired configurations when A is not
+ * 16-byte aligned with lda a multiple of 4. */
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);
