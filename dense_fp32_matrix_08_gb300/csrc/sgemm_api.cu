@@ -134,7 +134,8 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
                         int force_split) {
   struct Entry {
     int M, N, K, num_sms, force_v, force_split;
-    unsigned flags;  // alpha == 0, beta != 0, beta == 1, op(A) / op(B) transposed, TMA-able
+    unsigned flags;  // alpha == 0, beta != 0, beta == 1, op(A) / op(B) transposed, TMA-able,
+                     // planned with the device's measured cluster capacity
     bool valid;
     Plan plan;
   };
@@ -146,7 +147,8 @@ static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms,
                          (pr.transb ? 16u : 0u) | (pr.tma_ok ? 32u : 0u) |
                          (pr.kpair_ok ? 64u : 0u) | (pr.b_kmajor ? 128u : 0u) |
                          (pr.a_tma ? 256u : 0u) | (pr.b_tma ? 512u : 0u) |
-                         (pr.at_direct ? 1024u : 0u);
+                         (pr.at_direct ? 1024u : 0u) |
+                         (pr.cluster_cap != nullptr ? 2048u : 0u);  // measured capacity
   for (int i = 0; i < kEntries; ++i) {
     const Entry &e = cache[i];
     if (e.valid && e.M == pr.M && e.N == pr.N && e.K == pr.K && e.num_sms == num_sms &&
