@@ -56,8 +56,9 @@ static_assert(kTmaVariant == 26 && kFirstKpairVariant == 27 && kThinMVariant == 
 __device__ int g_ffma_status;
 
 // ------------------------------------------------------------------------------------
-// Per-device one-time setup: opt every kernel into its dynamic shared memory and cache
-// the SM count.
+// Per-device one-time setup: opt every kernel into its dynamic shared memory, cache the SM
+// count, and ask the driver how many CTAs each cluster-capable configuration keeps
+// resident in clusters of 2 .. 8 (the planner's cluster capacity).
 constexpr int kMaxDevices = 64;
 struct DeviceState {
   std::once_flag once;
@@ -129,7 +130,8 @@ cudaError_t device_setup(int *num_sms) {
 
 // make_plan evaluates a few hundred candidate layouts; a small per-thread cache keeps
 // repeated calls on the same shape at a table lookup. The plan depends only on the shape,
-// the special values of alpha and beta, the SM count and the forcing arguments.
+// the special values of alpha and beta, the operand flags, the SM count (and, when known,
+// the device's cluster capacity) and the forcing arguments.
 static Plan cached_plan(const Problem &pr, float alpha, float beta, int num_sms, int force_v,
                         int force_split) {
   struct Entry {
