@@ -285,6 +285,23 @@ static int run(const Problem &pr, const Plan &pl, float alpha, const float *A,
     tp.vec_c = vec_c ? 1 : 0;
     cudaError_t te;
     int parts = pl.split;  // partial tiles per C tile for the reduce kernel
+    if (pl.pack_a || pl.pack_b) {  // the small operand, copied to aligned rows for TMA
+      if (vs.thin < 5) return kErrBadVariant;  // (the planner makes no such plan)
+      if (pl.pack_a) {
+        pack_rows_kernel<<<grid_for_stream_kernel((long long)pr.M * ((pr.K + 3) / 4), num_sms),
+                           256, 0, stream>>>(A, pr.lda, pr.M, pr.K, ws, pl.lda_p);
+        tp.A = ws;
+        tp.lda = pl.lda_p;
+      } else {
+        pack_rows_kernel<<<grid_for_stream_kernel((long long)pr.K * ((pr.N + 3) / 4), num_sms),
+                           256, 0, stream>>>(B, pr.ldb, pr.K, pr.N, ws, pl.ldb_p);
+        tp.B = ws;
+        tp.ldb = pl.ldb_p;
+      }
+      tp.ws = reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + pl.pre_bytes);
+      te = cudaGetLastError();
+      if (te != cudaSuccess) return (int)te;
+    }
     if (vs.thin >= 5) {
       te = launch_thin_cluster(vs.thin == 6, tp, status_word(), stream);
       parts = 1;  // the cluster adds its slices itself

@@ -253,6 +253,24 @@ inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool bet
                               : (double)ctas / (double)(waves * slots);
   pl.cycles = std::max(compute, bytes / (2800.0 * fill)) + 3000.0 * (double)waves +
               2000.0 * pl.launches;
+  // The cluster kernels read both operands by TMA. A small operand whose rows TMA cannot
+  // address (row stride not a multiple of 16 bytes, or a misaligned base) is first copied
+  // to aligned rows in the workspace: at most 64 rows (thin-M: A) or columns (thin-N: B).
+  if (cluster && !(streams_b ? p.a_tma : p.b_tma)) {
+    if (streams_b) {
+      pl.pack_a = true;
+      pl.lda_p = ceil_div(p.K, 4) * 4;
+      pl.pack_a_bytes = (size_t)ceil_div((long long)p.M * pl.lda_p * 4, 256) * 256;
+    } else {
+      pl.pack_b = true;
+      pl.ldb_p = ceil_div(p.N, 4) * 4;
+      pl.pack_b_bytes = (size_t)ceil_div((long long)p.K * pl.ldb_p * 4, 256) * 256;
+    }
+    pl.pre_bytes = pl.pack_a_bytes + pl.pack_b_bytes;
+    pl.ws_bytes += pl.pre_bytes;
+    pl.launches += 1;
+    pl.cycles += 2.0 * small / 3400.0 + 2000.0;  // read and written once, one launch
+  }
   if (ctas > 0x7fffffffLL || pl.tiles_m > 65535 || pl.tiles_n > 65535 || split > 65535)
     pl.cycles = std::numeric_limits<double>::infinity();
   return pl;
@@ -502,8 +520,9 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
       if (force_v < 0 && (thin_n_kind ? p.N : p.M) > kThinMaxDim) continue;
       if (s.thin == 3 && (!p.b_tma || p.transa)) continue;  // B read by TMA as stored
       if (s.thin == 4 && (!p.a_tma || p.transb)) continue;  // A read by TMA as stored
-      if (s.thin >= 5) {  // cluster kernels: both operands read by TMA as stored
-        if (!p.a_tma || !p.b_tma || p.transa || p.transb) continue;
+      if (s.thin >= 5) {  // cluster kernels: both operands read by TMA, the streamed one as
+                          // stored, the small one as stored or from an aligned copy
+        if (!(s.thin == 5 ? p.b_tma : p.a_tma) || p.transa || p.transb) continue;
         if (force_split >= 1) {
           consider(model_thin(p, v, std::min(force_split, kMaxThinCluster), num_sms, beta_nz));
           continue;

@@ -178,11 +178,12 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
  * clamped so that every slice holds at least one K tile. The cluster thin kernels take
  * `split` as their cluster size, rounded up to 1, 2, 4 or 8. A TMA-fed configuration on
  * an operand TMA cannot address (lda or ldb not a multiple of 4, or a pointer not 16-byte
- * aligned) first copies it to aligned rows in the workspace. Returns -14 for an
+ * aligned) first copies it to aligned rows in the workspace; for the cluster thin kernels
+ * that copy is made of the small operand only (thin-M: A, thin-N: B). Returns -14 for an
  * out-of-range variant, for a configuration that cannot run the problem (a TMA-fed one on
- * transposed operands, see sgemm_f32_ex_forced; a TMA-fed thin one on an operand it reads
- * by TMA that TMA cannot address), and for the K-paired configurations when A is not
- * 16-byte aligned with lda a multiple of 4. */
+ * transposed operands, see sgemm_f32_ex_forced; a TMA-fed thin one whose streamed operand
+ * TMA cannot address), and for the K-paired configurations when A is not 16-byte aligned
+ * with lda a multiple of 4. */
 int sgemm_f32_forced(int M, int N, int K, float alpha, const float *A, int lda,
                      const float *B, int ldb, float beta, float *C, int ldc, int variant,
                      int split, cudaStream_t stream);

@@ -120,6 +120,25 @@ def test_plan_thin_shapes_use_thin_tiles_and_split_k():
             assert p["ws_bytes"] > 0
 
 
+def test_plan_thin_cluster_copies_an_unaligned_small_operand():
+    """A thin problem whose small operand TMA cannot read as stored (odd K for thin-M's A,
+    odd N for thin-N's B) still takes the cluster kernel: the small operand is copied to
+    aligned rows first (one more launch, a workspace of that copy's size). An unaligned
+    streamed operand rules the cluster kernels out, since copying it would double the
+    traffic of an HBM-bound kernel."""
+    M, N, K = 16, 4096, 4099
+    p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, 1.0, SMS)
+    assert p["variant"] == 43 and p["launches"] == 2
+    assert p["ws_bytes"] == -(-M * (-(-K // 4) * 4) * 4 // 256) * 256  # the copy of A only
+    M, N, K = 4096, 18, 2048
+    p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, 0.0, SMS)
+    assert p["variant"] == 44 and p["launches"] == 2
+    assert p["ws_bytes"] == -(-K * (-(-N // 4) * 4) * 4 // 256) * 256  # the copy of B only
+    for (M, N, K, lda, ldb) in ((16, 4097, 4096, 4096, 4097), (4096, 16, 8193, 8193, 16)):
+        p = sg.sgemm_f32_plan(M, N, K, lda, ldb, N, 1.0, 1.0, SMS)
+        assert p["variant"] not in THIN_CLUSTER, (M, N, K, p)
+
+
 def test_plan_small_cube_finishes_split_in_a_cluster():
     """256^3 splits every tile along K: the slices run as one cluster and add their partial
     tiles in shared memory, so the call is one launch with no workspace."""

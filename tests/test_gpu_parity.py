@@ -21,7 +21,7 @@ KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copi
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
 THIN_M_TMA = 41  # TMA-fed thin-M: B must be TMA-addressable
 THIN_N_TMA = 42  # TMA-fed thin-N: A must be TMA-addressable
-THIN_M_CL, THIN_N_CL = 43, 44  # cluster thin kernels: A and B must be TMA-addressable
+THIN_M_CL, THIN_N_CL = 43, 44  # cluster thin kernels: the streamed operand TMA-addressable
 TMA_THIN = (THIN_M_TMA, THIN_N_TMA, THIN_M_CL, THIN_N_CL)
 
 if torch.cuda.is_available():
@@ -231,6 +231,40 @@ def test_thin_cluster_sizes(thin_n, cluster, beta):
         assert_bound(out.numpy(), R, S, beta, C.numpy(), f"v{v} S{cluster} {M,N,K}")
         again, _ = _run(A, B, C, 1.5, beta, *lds, variant=v, split=cluster)
         assert torch.equal(out, again), (M, N, K)
+
+
+def _odd_ld(x):
+    """A row stride of at least x elements that is not a multiple of 4 (16 bytes)."""
+    return x + 1 if (x + 1) % 4 else x + 2
+
+
+@pytest.mark.parametrize("thin_n", [False, True])
+@pytest.mark.parametrize("cluster", [0, 1, 4, 8])
+def test_thin_cluster_small_operand_copied(thin_n, cluster):
+    """The cluster thin kernels when the small operand cannot be read by TMA as stored (a
+    row stride that is not a multiple of 16 bytes and a misaligned base): it is first
+    copied to aligned rows in the workspace, and the streamed operand is read as stored.
+    Cluster 0 is the automatic plan, checked when the model takes the cluster kernel."""
+    for (M, N, K) in [(16, 4096, 4099), (5, 1000, 777), (33, 4100, 2051)]:
+        if thin_n:
+            M, N = N, M
+        A, B, C = make_inputs(M, N, K, seed=M + 5 * N + 3 * K + cluster)
+        if thin_n:  # streamed A aligned; small B (N wide) at an odd stride and offset
+            lds, offs = (-(-K // 4) * 4, _odd_ld(N), N + 1), (0, 1, 2)
+        else:       # streamed B aligned; small A (K wide) at an odd stride and offset
+            lds, offs = (_odd_ld(K), -(-N // 4) * 4, N + 1), (3, 0, 2)
+        v = THIN_N_CL if thin_n else THIN_M_CL
+        if cluster == 0:
+            plan = sg.sgemm_f32_plan(M, N, K, *lds, 0.75, -1.25)
+            if plan["variant"] != v:
+                continue  # the model prefers another kernel for this shape
+            assert plan["ws_bytes"] > 0 and plan["launches"] == 2, plan
+            out, guard = _run(A, B, C, 0.75, -1.25, *lds, offs=offs)
+        else:
+            out, guard = _run(A, B, C, 0.75, -1.25, *lds, offs=offs, variant=v, split=cluster)
+        assert guard, (M, N, K)
+        R, S = oracle.sgemm_f64(A, B, C, 0.75, -1.25)
+        assert_bound(out.numpy(), R, S, -1.25, C.numpy(), f"v{v} S{cluster} copied {M,N,K}")
 
 
 CLUSTER_SPLIT_VARIANTS = (2, 12, 32, 35, 37)  # copy-fed and TMA-fed (A as stored / k-major)

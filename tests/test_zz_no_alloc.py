@@ -43,11 +43,11 @@ ERR_TOO_SMALL = _header_int("SGEMM_F32_ERR_SCRATCH_TOO_SMALL")
 
 
 @pytest.mark.parametrize("M,N,K,alpha,beta,seed", [
-    # thin M with an A that TMA cannot address (lda = 4099): every tile split along K and
-    # finished from the workspace (an addressable A takes the cluster kernel, no workspace)
+    # thin M with an A that TMA cannot address (lda = 4099): the cluster kernel reads an
+    # aligned copy of A made in the scratch
     (16, 4096, 4099, 1.0, 1.0, 41),
     (2100, 2600, 300, 1.5, 0.5, 42),    # whole waves plus a split last wave
-    (4096, 18, 2048, -0.75, 0.0, 43),   # thin N (ldb = 18: split-K kernel), beta = 0
+    (4096, 18, 2048, -0.75, 0.0, 43),   # thin N, ldb = 18: an aligned copy of B; beta = 0
 ])
 def test_noalloc_matches_sgemm_f32_twice(M, N, K, alpha, beta, seed):
     import dense_fp32_matrix_08_gb300 as sg
