@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle sample")
     ap.add_argument("--no-variants", action="store_true",
                     help="skip the separately reported tensor-core 3xTF32 variant")
@@ -257,7 +257,9 @@ def cpu_oracle_sample(w, A, B, C, seconds: float, rows_hint: int | None = None):
     """Time the oracle on a bounded set of rows; returns (TFLOP/s, rows, seconds, R, S)."""
     import oracle
     rng = np.random.default_rng(12345)
-    probe = np.sort(rng.choice(w.M, size=min(w.M, 4), replace=False))
+    # the oracle spreads rows over its threads: probe with two rows per thread, so that
+    # the per-row time it measures is the one the full sample runs at
+    probe = np.sort(rng.choice(w.M, size=min(w.M, 2 * oracle.threads()), replace=False))
     t0 = time.perf_counter()
     oracle.sgemm_f64_rows(A, B, C, w.alpha, w.beta, probe)
     dt = max(time.perf_counter() - t0, 1e-6)
