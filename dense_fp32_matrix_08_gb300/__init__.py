@@ -22,7 +22,8 @@ __all__ = [
     "sgemm_f32_colmajor", "sgemv_f32", "sdot_f32", "sgemm_f32_status", "sgemm_f32_3xtf32",
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
     "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
-    "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm", "EXPORTED",
+    "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm_f32_wait_selftest",
+    "sgemm_f32_release_workspace", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -34,7 +35,7 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status",
             "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
             "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load",
-            "sgemm_f32_host", "sgemm_f32_wait_selftest")
+            "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm_f32_release_workspace")
 
 
 class SgemmError(RuntimeError):
@@ -75,6 +76,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_3xtf32_status.argtypes = [pi]
     L.sgemm_f32_status.argtypes = [pi]
     L.sgemm_f32_wait_selftest.argtypes = [pi, ctypes.POINTER(ctypes.c_float)]
+    L.sgemm_f32_release_workspace.argtypes = [psz]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
@@ -248,6 +250,14 @@ def sgemm_f32_wait_selftest() -> dict:
     t, sec = ctypes.c_int(0), ctypes.c_float(0.0)
     rc = lib.sgemm_f32_wait_selftest(ctypes.byref(t), ctypes.byref(sec))
     return {"status": rc, "timed_out": t.value, "seconds": sec.value}
+
+
+def sgemm_f32_release_workspace() -> tuple[int, int]:
+    """(call status, bytes returned): hand the library pool's cached device memory on the
+    current device back to the system (see the header)."""
+    n = ctypes.c_size_t(0)
+    rc = lib.sgemm_f32_release_workspace(ctypes.byref(n))
+    return rc, n.value
 
 
 def sgemm_f32_3xtf32_status() -> tuple[int, int]:

@@ -638,6 +638,22 @@ int sgemm_f32_wait_selftest(int *timed_out, float *seconds) {
   return 0;
 }
 
+int sgemm_f32_release_workspace(size_t *released_bytes) {
+  if (released_bytes) *released_bytes = 0;
+  int num_sms = 0;
+  cudaError_t e = device_setup(&num_sms);  // (creates the empty pool on a first call)
+  if (e != cudaSuccess) return (int)e;
+  cudaMemPool_t pool = workspace_pool();
+  if (pool == nullptr) return (int)cudaErrorInvalidDevice;
+  uint64_t before = 0, after = 0;
+  e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &before);
+  if (e == cudaSuccess) e = cudaMemPoolTrimTo(pool, 0);
+  if (e == cudaSuccess) e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &after);
+  if (e != cudaSuccess) return (int)e;
+  if (released_bytes) *released_bytes = (size_t)(before > after ? before - after : 0);
+  return 0;
+}
+
 int sgemm_f32_status(int *status) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_ffma_status, sizeof(int));

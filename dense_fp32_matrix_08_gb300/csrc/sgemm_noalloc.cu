@@ -4,6 +4,7 @@
 // instead of memory from cudaMallocAsync.
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "../../include/sgemm_f32.h"
@@ -20,26 +21,33 @@ static __device__ __align__(256) float g_scratch[kScratchBytes / sizeof(float)];
 
 constexpr int kMaxDevices = 64;
 struct ScratchSlot {
-  std::once_flag once;
-  void *ptr = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  std::atomic<void *> ptr{nullptr};  // set once a lookup has succeeded
 };
 ScratchSlot g_slots[kMaxDevices];
 
-// Device address of g_scratch on the current device, looked up on the first call that
-// runs on that device (with that device current).
+// Device address of g_scratch on the current device, looked up (with that device current)
+// by the first call on the device that succeeds. A failed lookup, for example one made while
+// a stream capture forbids it, is not remembered: the next call tries again.
 cudaError_t scratch_on_current_device(void **ptr) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
   ScratchSlot &slot = g_slots[dev];
-  std::call_once(slot.once, [&slot]() {
-    slot.err = cudaGetSymbolAddress(&slot.ptr, g_scratch);
-    if (slot.err == cudaSuccess && slot.ptr == nullptr) slot.err = cudaErrorInvalidSymbol;
-  });
-  *ptr = slot.ptr;
-  return slot.err;
+  void *p = slot.ptr.load(std::memory_order_acquire);
+  if (p == nullptr) {
+    std::lock_guard<std::mutex> lock(slot.mu);
+    p = slot.ptr.load(std::memory_order_relaxed);
+    if (p == nullptr) {
+      e = cudaGetSymbolAddress(&p, g_scratch);
+      if (e != cudaSuccess) return e;
+      if (p == nullptr) return cudaErrorInvalidSymbol;
+      slot.ptr.store(p, std::memory_order_release);
+    }
+  }
+  *ptr = p;
+  return cudaSuccess;
 }
 
 }  // namespace

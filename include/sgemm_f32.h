@@ -26,13 +26,21 @@
  *   A, B and C are device pointers owned by the caller (any memory the GPU can address with
  *   a plain load: cudaMalloc, cudaMallocAsync, managed). The library keeps no pointer after
  *   the call returns. C must not overlap A or B.
- *   sgemm_f32 may allocate a workspace (split-K partial tiles, at most 64 MiB, plus aligned
- *   copies of A and B when lda or ldb is not a multiple of 4 or a pointer is not 16-byte
- *   aligned, at most 2 GiB) with a stream-ordered
- *   allocation on `stream` and free it on the same stream before returning. It comes from
- *   a memory pool the library creates per device, which keeps freed memory for reuse until
- *   the process exits. sgemm_f32_workspace_size() reports the size; sgemm_f32_ws() takes
- *   a caller-provided workspace instead.
+ *   sgemm_f32 may allocate a workspace with a stream-ordered allocation on `stream` and
+ *   free it on the same stream before returning. It holds, at its front, the copies that
+ *   pre-pass kernels make before the GEMM kernel runs, and behind them split-K partial
+ *   tiles (at most 64 MiB):
+ *     - A^T, a K x ceil4(M) copy of A (4 * K * ceil4(M) bytes), for the plans that read A
+ *       k-major: the automatic plan of every large aligned problem (268 MB at 8192^3,
+ *       67 MB at 4096^3);
+ *     - aligned copies of A and B (ld rounded up to a multiple of 4) when lda or ldb is not
+ *       a multiple of 4 or a pointer is not 16-byte aligned;
+ *   the pre-pass copies together are at most 2 GiB. The workspace comes from a memory pool
+ *   the library creates per device. The pool keeps freed memory for reuse, so a repeated
+ *   call does not map memory again; it holds the largest workspace a call has needed (more
+ *   when calls on several streams overlap) until sgemm_f32_release_workspace() returns it
+ *   or the process exits. sgemm_f32_workspace_size() reports the size a call needs;
+ *   sgemm_f32_ws() takes a caller-provided workspace instead.
  *
  * Asynchrony
  *   Every compute call enqueues its kernels on `stream` (0 = the legacy default stream) and
@@ -229,7 +237,10 @@ int sgemm_f32_ex_forced(int transa, int transb, int M, int N, int K, float alpha
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current. Make that first call on a device before
- * any stream capture on it.
+ * any stream capture on it; a lookup that fails is returned as its cudaError_t and tried
+ * again by the next call. Like any first library call on a device, the first call also
+ * creates the library's per-device memory pool, empty; this entry point takes nothing from
+ * it.
  *
  * Sharing: all calls in the process share the one array of a device, which keeps whatever
  * the last call left in it. Calls ordered on the GPU (the same stream, or streams ordered by
@@ -274,6 +285,16 @@ int sgemm_f32_3xtf32_workspace_size(int M, int N, int K, size_t *bytes);
  * legacy stream): 0 = fine; 1, 2, 3 = a bounded wait of the producer, MMA or epilogue
  * threads gave up (the kernel then skipped work and the result is not valid). */
 int sgemm_f32_3xtf32_status(int *status);
+
+/* Returns to the system the device memory that the library's pool on the current device
+ * keeps for reuse: workspaces freed by earlier calls of every entry point (sgemm_f32 and
+ * its variants, the host-buffer, 3xTF32, SGEMV / SDOT and autotune calls). Memory that a
+ * call still uses is kept, and so is memory whose stream-ordered free has not yet run on
+ * the GPU: synchronise the streams that ran library calls first to release everything.
+ * Later calls allocate again as needed. *released_bytes (may be NULL) = bytes returned.
+ * The first library call on a device creates its (empty) pool, so a first call here does.
+ * Returns 0 or a cudaError_t. */
+int sgemm_f32_release_workspace(size_t *released_bytes);
 
 /* Reads and clears the device status word of the TMA-fed FFMA kernel (synchronising copy
  * on the legacy stream): 0 = fine; 1 or 2 = a bounded mbarrier wait gave up (a consumer

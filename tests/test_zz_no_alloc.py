@@ -68,10 +68,12 @@ def test_noalloc_matches_sgemm_f32_twice(M, N, K, alpha, beta, seed):
         assert sg.sgemm_f32_noalloc(M, N, K, alpha, dA, K, dB, N, beta, dC, N) == 0
         torch.cuda.synchronize()
         out = dC.cpu()
-        # against the existing entry point, with the parity tests' bound ...
+        # the same plan and kernels as sgemm_f32, whatever the scratch held before ...
+        assert torch.equal(out, ref), f"noalloc call {call} is not bitwise sgemm_f32's"
+        # ... within the parity tests' bound of the existing entry point ...
         assert_bound(out.numpy(), ref.numpy().astype(np.float64), tol_S, beta, C.numpy(),
                      f"noalloc call {call} vs sgemm_f32")
-        # ... and both against the oracle
+        # ... and against the oracle
         assert_bound(out.numpy(), R, S, beta, C.numpy(), f"noalloc call {call} vs oracle")
 
 
