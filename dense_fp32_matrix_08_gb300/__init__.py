@@ -289,11 +289,16 @@ def sgemm_f32_num_variants() -> int:
 
 
 def sgemm_f32_variant_info(v: int) -> dict | None:
+    """Shape of tile configuration v, with "built" False for a configuration kept in the
+    table but not compiled (forcing it returns -14); None when v is out of range."""
     vals = [ctypes.c_int(0) for _ in range(7)]
-    if lib.sgemm_f32_variant_info(v, *[ctypes.byref(x) for x in vals]) != 0:
+    rc = lib.sgemm_f32_variant_info(v, *[ctypes.byref(x) for x in vals])
+    if rc not in (0, 1):
         return None
     keys = ("BM", "BN", "BK", "threads", "TM", "TN", "stages")
-    return dict(zip(keys, (x.value for x in vals)))
+    info = dict(zip(keys, (x.value for x in vals)))
+    info["built"] = rc == 0
+    return info
 
 
 def sgemm_f32_version() -> str:

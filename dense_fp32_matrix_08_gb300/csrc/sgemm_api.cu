@@ -22,8 +22,18 @@
 
 namespace sgemm {
 
+// The copy-fed kernels of configuration V, or none for a retired configuration.
+template <int V>
+VariantKernels kernels_if_built() {
+  if constexpr (variant_built(V)) {
+    return variant_kernels<V>();
+  } else {
+    return VariantKernels{};
+  }
+}
+
 static const VariantKernels kKernels[kNumVariants] = {
-#define SGEMM_KERNELS_ENTRY(v) variant_kernels<v>(),
+#define SGEMM_KERNELS_ENTRY(v) kernels_if_built<v>(),
     SGEMM_FOR_EACH_VARIANT(SGEMM_KERNELS_ENTRY)
 #undef SGEMM_KERNELS_ENTRY
     VariantKernels{},  // kTmaVariant: its own kernel (sgemm_tma.cu)
@@ -589,6 +599,7 @@ int sgemm_f32_num_variants(void) { return kNumVariants; }
 int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *TM, int *TN,
                            int *stages) {
   if (v < 0 || v >= kNumVariants) return -1;
+  const int built = variant_built(v) ? 0 : 1;
   const VariantShape &s = kVariants[v];
   if (BM) *BM = s.BM;
   if (BN) *BN = s.BN;
@@ -597,7 +608,7 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
   if (TM) *TM = s.TM;
   if (TN) *TN = s.TN;
   if (stages) *stages = s.stages;
-  return 0;
+  return built;
 }
 
 const char *sgemm_f32_version(void) { return "sgemm_f32 0.1.0 sm_103a"; }

@@ -103,10 +103,13 @@ constexpr VariantShape kVariants[] = {
     {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1), 1.06, true, false, true, false, 4, 0, true, 37},
     {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 1.04, true, false, true, false, 5, 0, true, 38},
     // 37, 38: the same two shapes reading A as stored and transposing each A tile in shared
-    // memory (no workspace, no pre-pass; ~3% slower than 35 / 36); 128 x 128 with 2 stages
-    // to fit 2 CTAs/SM
-    {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1) + 16384, 1.028, true, false, true, false, 6},
-    {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1) + 16384, 1.03, true, false, true, false, 7},
+    // memory (no workspace, no pre-pass; 128 x 128 with 2 stages to fit 2 CTAs/SM). They
+    // are 3-5% slower than 35 / 36 at 8192^3 and 14-34% slower than the automatic choice
+    // without them at 768^3 and 1536^3 (measured per call), so they are not automatic: they
+    // are the twins that sgemm_f32_ws and sgemm_f32_noalloc take when their workspace cannot
+    // hold the A^T copy
+    {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1) + 16384, 1.028, false, false, true, false, 6},
+    {128, 128, 32, 128, 8, 16, 2, 2, 1, smem_of(128, 128, 32, 2, 1) + 16384, 1.03, false, false, true, false, 7},
     // 39, 40: k-major A, 128 x 64 at 4 CTAs/SM and 128 x 128 with 2 stages. 39 is automatic
     // with its efficiency calibrated against 35 (1.8% slower at 8192^3, 13% faster at 3000^3,
     // 6% at 2048^3, where its 608 slots round the waves better)
@@ -129,6 +132,24 @@ constexpr VariantShape kVariants[] = {
     {128, 64, 32, 128, 8, 8, 2, 3, 1, smem_of(128, 64, 32, 2, 1) + 16384, 0.98, false, false, true, false, 10},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
+
+// Copy-fed configurations that stay in the table, so that every index keeps its meaning, but
+// are not compiled: neither the automatic plan nor sgemm_f32_autotune chose any of them on
+// the shapes measured (the copy-fed configurations the plan can choose are 0-5, 8, 13, 16
+// and 21). Forcing one returns -14.
+constexpr int kRetiredVariants[] = {6, 7, 9, 10, 11, 12, 14, 15, 17, 18, 19, 20, 22, 23, 24, 25};
+constexpr bool variant_built(int v) {
+  for (int r : kRetiredVariants)
+    if (r == v) return false;
+  return v >= 0 && v < kNumVariants;
+}
+constexpr bool retired_are_forced_only() {
+  for (int r : kRetiredVariants)
+    if (kVariants[r].automatic || kVariants[r].trans_ok || kVariants[r].tma || kVariants[r].thin)
+      return false;
+  return true;
+}
+static_assert(retired_are_forced_only(), "only forced-only copy-fed configurations retire");
 constexpr int kTmaVariant = 26;
 constexpr int kFirstKpairVariant = 27;
 constexpr int kThinMVariant = 33, kThinNVariant = 34;
@@ -499,6 +520,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
   const int v_hi = force_v >= 0 ? force_v : kNumVariants - 1;
   const bool trans = p.transa || p.transb;
   for (int v = v_lo; v <= v_hi; ++v) {
+    if (!variant_built(v)) continue;
     if (force_v < 0 && !kVariants[v].automatic) continue;
     const bool at_path = kVariants[v].at && p.at_direct && !p.transb;  // A_st is A^T
     if (trans && !kVariants[v].trans_ok && !at_path) continue;

@@ -172,7 +172,9 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
 int sgemm_f32_num_variants(void);
 
 /* Describe variant v: CTA tile BM x BN x BK, threads per CTA, per-thread TM x TN
- * accumulator tile, pipeline stages. Returns 0, or -1 if v is out of range. */
+ * accumulator tile, pipeline stages. Returns 0; 1 for a configuration that keeps its index
+ * in the table but is not compiled into this build (the outputs are still filled; forcing
+ * it returns -14); or -1 if v is out of range. */
 int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *TM,
                            int *TN, int *stages);
 

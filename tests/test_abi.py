@@ -92,6 +92,24 @@ def test_variant_table():
     assert big["TM"] * big["TN"] >= 64  # at least an 8x8 register outer product
 
 
+RETIRED = (6, 7, 9, 10, 11, 12, 14, 15, 17, 18, 19, 20, 22, 23, 24, 25)
+
+
+def test_retired_variants_are_described_not_built():
+    for v in range(sg.sgemm_f32_num_variants()):
+        assert sg.sgemm_f32_variant_info(v)["built"] == (v not in RETIRED), v
+
+
+def test_shared_memory_transpose_twins_are_not_automatic():
+    """Configurations 37 and 38 (A transposed in the CTA) were measured slower than the
+    automatic choice without them at 768^3 and 1536^3 (and 3-5% behind their k-major
+    counterparts at 8192^3): the automatic plan never takes them."""
+    for n in (512, 768, 1024, 1280, 1536, 1792, 2048, 3000, 4096, 8192):
+        assert _plan(n, n, n, beta=0.5)["variant"] not in (37, 38), n
+    for shp in [(1500, 1500, 4000), (4096, 1024, 2048), (4099, 3001, 777)]:
+        assert _plan(*shp, beta=0.5)["variant"] not in (37, 38), shp
+
+
 def _plan(M, N, K, beta=1.0):
     p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, beta, SMS)
     assert p["status"] == 0

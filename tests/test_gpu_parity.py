@@ -15,7 +15,10 @@ from workloads import BY_NAME, CONFIGS, make_inputs, workload_inputs
 from parity_util import assert_bound, guard_intact, to_device_view
 
 pytestmark = pytest.mark.gpu
-NUM_VARIANTS = 46  # compiled tile configurations; checked against the library below
+NUM_VARIANTS = 46  # tile configurations in the table; checked against the library below
+# configurations kept in the table but not compiled (forcing one returns -14)
+RETIRED = (6, 7, 9, 10, 11, 12, 14, 15, 17, 18, 19, 20, 22, 23, 24, 25)
+BUILT = tuple(v for v in range(NUM_VARIANTS) if v not in RETIRED)
 TMA_VARIANTS = (26, 30, 31, 32, 35, 36, 37, 38, 39, 40, 45)  # every TMA-fed instance
 KPAIR_VARIANTS = (27, 28, 29)  # K-paired TMA-fed kernel: aligned A, any B (copied to B^T)
 THIN_M, THIN_N = 33, 34  # streaming kernels for thin products
@@ -101,14 +104,16 @@ def test_config_sampled(name):
 # Every variant, aligned and unaligned, with and without split-K, across ragged tiles.
 
 def _variants():
-    return list(range(sg.sgemm_f32_num_variants())) if torch.cuda.is_available() else []
+    """Every compiled configuration (retired ones are refused, see test_retired_variant_is_refused)."""
+    return [v for v in range(sg.sgemm_f32_num_variants()) if v not in RETIRED] \
+        if torch.cuda.is_available() else []
 
 
 RAGGED = [(1, 1, 1), (3, 5, 7), (17, 13, 9), (127, 129, 33), (129, 257, 65),
           (255, 31, 100), (16, 300, 257), (300, 16, 129), (257, 255, 1)]
 
 
-@pytest.mark.parametrize("variant", range(NUM_VARIANTS))
+@pytest.mark.parametrize("variant", BUILT)
 @pytest.mark.parametrize("split", [1, 3, -1])
 @pytest.mark.parametrize("aligned", [True, False])
 def test_variant_ragged(variant, split, aligned):
@@ -267,7 +272,7 @@ def test_thin_cluster_small_operand_copied(thin_n, cluster):
         assert_bound(out.numpy(), R, S, -1.25, C.numpy(), f"v{v} S{cluster} copied {M,N,K}")
 
 
-CLUSTER_SPLIT_VARIANTS = (2, 12, 32, 35, 37)  # copy-fed and TMA-fed (A as stored / k-major)
+CLUSTER_SPLIT_VARIANTS = (2, 13, 32, 35, 37)  # copy-fed and TMA-fed (A as stored / k-major)
 
 
 @pytest.mark.parametrize("variant", CLUSTER_SPLIT_VARIANTS)
@@ -294,6 +299,16 @@ def test_cluster_split_finish(variant, split, beta):
 
 def test_variant_count():
     assert sg.sgemm_f32_num_variants() == NUM_VARIANTS
+
+
+@pytest.mark.parametrize("variant", RETIRED)
+def test_retired_variant_is_refused(variant):
+    """A configuration kept in the table but not compiled is refused without a launch."""
+    A = torch.ones((64, 64), device="cuda")
+    C = torch.full((64, 64), 3.0, device="cuda")
+    assert sg.sgemm_f32_forced(64, 64, 64, 1.0, A, 64, A, 64, 1.0, C, 64, variant, 1) == -14
+    torch.cuda.synchronize()
+    assert bool((C == 3.0).all())
 
 
 def test_tma_variants_on_unaligned_and_transposed_operands():
@@ -403,9 +418,18 @@ def test_deterministic_and_ws_entry_match():
         dA, _ = to_device_view(A)
         dB, _ = to_device_view(B)
         dC, _ = to_device_view(C)
+        # too small for the partial tiles alone (an A^T copy in the plan has a twin that
+        # does without it; the partials have none)
+        at_copy = 0
+        if p["variant"] in (35, 36, 39, 40):
+            at_copy = -(-4 * K * (-(-M // 4) * 4) // 256) * 256
+        short = p["ws_bytes"] - at_copy - 1
         ws = torch.empty(p["ws_bytes"], dtype=torch.uint8, device="cuda")
+        before = dC.clone()
         assert sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, dC, N, ws.data_ptr(),
-                               p["ws_bytes"] - 1) == -13
+                               short) == -13
+        torch.cuda.synchronize()
+        assert torch.equal(dC, before)
 
 
 def test_illegal_arguments_launch_nothing():

@@ -103,7 +103,7 @@ def test_noalloc_without_scratch_need():
     """A plan without split-K runs without touching the scratch at all."""
     import dense_fp32_matrix_08_gb300 as sg
 
-    M, N, K = 2432, 2048, 256  # exactly one wave of 128 x 256 tiles on 152 SMs
+    M, N, K = 2432, 2432, 64  # short K: whole tiles, no split-K, no pre-pass copy
     p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, 0.0, 0)
     if p["ws_bytes"] != 0:
         pytest.skip("plan on this device uses split-K for this shape")
