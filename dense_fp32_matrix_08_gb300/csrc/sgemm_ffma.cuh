@@ -65,6 +65,24 @@ struct GemmParams {
 // ------------------------------------------------------------------------------------
 // PTX wrappers (cp.async family, available sm_80+; compiled here for sm_103a).
 
+// Programmatic dependent launch: wait until the grids this one depends on (the previous
+// kernel in the stream, when this kernel was launched with programmatic stream
+// serialization) have completed and their memory is visible. A no-op otherwise. Called
+// before the kernel's first global-memory access, so that a launch may start while the
+// previous kernel is finishing without reading anything it has not yet written.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
+
+// Programmatic dependent launch: this CTA no longer needs its SM for the main loop, so the
+// next kernel in the stream (if launched with programmatic stream serialization) may be
+// scheduled once every CTA of this grid has called this or exited. Only a scheduling hint:
+// the next kernel's griddep_wait() still waits for this grid to complete, epilogue stores
+// included. Called after the main loop, so the next kernel's prologue overlaps the epilogue.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -306,6 +324,7 @@ __device__ __forceinline__ void tile_coords(int bid, int tiles_m, int tiles_n, i
 template <class Cfg, int APATH, int BPATH>
 __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     sgemm_ffma_kernel(const GemmParams p) {
+  griddep_wait();  // (launched with programmatic dependent launch: see launch_1d)
   static_assert(APATH == APATH_N || Cfg::MODE != 2, "duplicated-A layout needs A row-major");
   static_assert(APATH != APATH_T16 || (Cfg::BK * Cfg::BM / 4) % Cfg::NT == 0, "A^T 16B tiling");
   static_assert(APATH != APATH_T4 || (Cfg::BK * Cfg::BM) % Cfg::NT == 0, "A^T 4B tiling");
@@ -561,6 +580,7 @@ __global__ void __launch_bounds__(Cfg::NT, Cfg::MIN_BLOCKS)
     }
   }
   cp_async_wait<0>();
+  griddep_launch_dependents();
 
   // ---- epilogue -----------------------------------------------------------------------
   // Thread element (i, j) of the tile sits at row warp_m*WM + (i/4)*LM*4 + lane_m*4 + i%4

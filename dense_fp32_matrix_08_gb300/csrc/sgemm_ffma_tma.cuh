@@ -118,8 +118,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
       mbar_init(bars + 8 * (STAGES + s), THREADS / 32);
     }
     mbar_init_fence();
+    tma_prefetch_map(&map_a);
+    tma_prefetch_map(&map_b);
   }
   __syncthreads();
+  // The launch allows programmatic dependent launch (launch_1d): everything above touches
+  // only shared memory and the kernel's parameters, so it may overlap the previous
+  // kernel's last CTAs; from here on the previous kernel's writes are visible.
+  griddep_wait();
 
   auto issue = [&](int kt) {  // thread 0 only
     const int s = kt % STAGES;
@@ -134,8 +140,6 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
   };
   int issued = 0;
   if (tid == 0) {
-    tma_prefetch_map(&map_a);
-    tma_prefetch_map(&map_b);
     for (int kt = 0; kt < STAGES - 1 && kt < KT; ++kt) issue(kt);
     issued = min(STAGES - 1, KT);
   }
@@ -273,6 +277,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
     __syncwarp();
     if (lane == 0) mbar_arrive(bars + 8 * (STAGES + s));  // this warp is done with stage s
   }
+  griddep_launch_dependents();
   // Thread 0 may not leave while copies it issued are in flight: wait for the last ones.
   if (tid == 0) {
     for (int kt = issued - 1; kt >= 0 && kt >= issued - STAGES; --kt)

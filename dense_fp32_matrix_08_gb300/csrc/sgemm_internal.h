@@ -28,7 +28,9 @@ struct GemmParams;
 struct Problem;
 
 // Launch `kernel` on a 1-D grid, in thread-block clusters of `cluster` CTAs along x when
-// cluster > 1 (grid a multiple of it), else as a plain launch.
+// cluster > 1 (grid a multiple of it), else as a plain launch. The launch allows
+// programmatic dependent launch: its CTAs may be scheduled while the previous kernel in
+// the stream finishes, so `kernel` must call griddep_wait() before touching global memory.
 template <class... KArgs, class... Args>
 cudaError_t launch_1d(void (*kernel)(KArgs...), int grid, int threads, size_t smem,
                       int cluster, cudaStream_t stream, Args &&...args) {
@@ -37,13 +39,15 @@ cudaError_t launch_1d(void (*kernel)(KArgs...), int grid, int threads, size_t sm
   cfg.blockDim = dim3((unsigned)threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = (unsigned)(cluster > 1 ? cluster : 1);
-  attr.val.clusterDim.y = 1;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = cluster > 1 ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)(cluster > 1 ? cluster : 1);
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = cluster > 1 ? 2 : 1;
   if (cluster > 1 && grid % cluster != 0) return cudaErrorInvalidConfiguration;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
 }

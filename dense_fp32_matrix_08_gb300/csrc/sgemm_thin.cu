@@ -98,13 +98,17 @@ cudaError_t launch_thin_cluster(bool thin_n, const thin::ThinParams &p, int *sta
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr;
-  attr.id = cudaLaunchAttributeClusterDimension;
-  attr.val.clusterDim.x = 1;
-  attr.val.clusterDim.y = S;
-  attr.val.clusterDim.z = 1;
-  cfg.attrs = &attr;
-  cfg.numAttrs = S > 1 ? 1 : 0;
+  // programmatic dependent launch (the kernel waits for the previous grid before any
+  // global access), and the cluster of the K slices
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = 1;
+  attr[1].val.clusterDim.y = S;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = S > 1 ? 2 : 1;
   if (thin_n)
     return cudaLaunchKernelEx(&cfg, thin::thin_cluster_kernel<true>, map_big, map_small, p,
                               status);

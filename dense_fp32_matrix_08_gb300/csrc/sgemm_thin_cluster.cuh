@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(cl::THREADS, 1)
     thin_cluster_kernel(const __grid_constant__ CUtensorMap map_big,
                         const __grid_constant__ CUtensorMap map_small, const ThinParams p,
                         int *status) {
+  griddep_wait();  // (launched with programmatic dependent launch: see launch_thin_cluster)
   using namespace cl;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = saddr(smem_raw);
@@ -218,6 +219,7 @@ __global__ void __launch_bounds__(cl::THREADS, 1)
     __syncwarp();  // every lane has read the stage (and tb) before they are refilled
     if (lane == 0 && j + SPW < my_chunks) issue(j + SPW);
   }
+  griddep_launch_dependents();
   // No copy may still be writing the rings when they are reused below: a warp that stopped
   // early waits (bounded) for the copies it issued and has not seen complete.
   if (lane == 0) {

@@ -45,6 +45,10 @@
  * Asynchrony
  *   Every compute call enqueues its kernels on `stream` (0 = the legacy default stream) and
  *   returns without waiting. Results are visible after the stream is synchronised.
+ *   The GEMM kernels are launched with programmatic dependent launch. Their CTAs may be
+ *   scheduled while the previous kernel on `stream` finishes. Each one waits for that
+ *   kernel to complete (and its writes to be visible) before it reads or writes global
+ *   memory, so stream order is the same as for plain launches, under stream capture too.
  *
  * Scalars and special cases (BLAS reference conventions)
  *   alpha and beta are host floats passed by value.
