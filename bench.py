@@ -622,6 +622,19 @@ def our_arm(args, dist: Dist):
                 "kernel_launches_per_step": plan["launches"],
                 "fp32": {"achieved": achieved, "peak": peak, "unit": "TFLOP/s"}}
 
+    # the derived FP32 peak's measured counterpart: the library's FFMA2 pipe probe, timed
+    # after (outside) the timed region
+    probe = sg.sgemm_f32_fma_probe(1 << 17, 5)
+    if probe["status"] == 0 and probe["tflops"] > 0:
+        fp32 = roof.get("fp32", roof)
+        fp32["fp32_probe"] = {
+            "tflops": probe["tflops"], "ms_per_launch": probe["ms"],
+            "frac_of_derived_peak": probe["tflops"] / peak,
+            "what": "sgemm_f32_fma_probe: SMs x 4 CTAs x 256 threads, 16 independent "
+                    "fma.rn.f32x2 chains per thread, 2^17 iterations; median of 5 launches "
+                    "(CUDA events), run after the timed region"}
+        fp32["frac_of_probe"] = achieved / probe["tflops"]
+
     # end to end: host buffers in pinned memory through the library's host-buffer entry
     # point; the copies in and out are inside the timed region
     e2e = None

@@ -23,7 +23,7 @@ __all__ = [
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
     "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
     "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm_f32_wait_selftest",
-    "sgemm_f32_release_workspace", "sgemm", "EXPORTED",
+    "sgemm_f32_release_workspace", "sgemm_f32_fma_probe", "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -35,7 +35,8 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status",
             "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
             "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load",
-            "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm_f32_release_workspace")
+            "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm_f32_release_workspace",
+            "sgemm_f32_fma_probe")
 
 
 class SgemmError(RuntimeError):
@@ -77,6 +78,8 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_status.argtypes = [pi]
     L.sgemm_f32_wait_selftest.argtypes = [pi, ctypes.POINTER(ctypes.c_float)]
     L.sgemm_f32_release_workspace.argtypes = [psz]
+    L.sgemm_f32_fma_probe.argtypes = [i, i, ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_float)]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
@@ -250,6 +253,13 @@ def sgemm_f32_wait_selftest() -> dict:
     t, sec = ctypes.c_int(0), ctypes.c_float(0.0)
     rc = lib.sgemm_f32_wait_selftest(ctypes.byref(t), ctypes.byref(sec))
     return {"status": rc, "timed_out": t.value, "seconds": sec.value}
+
+
+def sgemm_f32_fma_probe(iters: int = 1 << 17, reps: int = 5) -> dict:
+    """Measure the FP32 FMA pipe: {"status", "tflops", "ms"} (see the header)."""
+    t, ms = ctypes.c_double(0.0), ctypes.c_float(0.0)
+    rc = lib.sgemm_f32_fma_probe(iters, reps, ctypes.byref(t), ctypes.byref(ms))
+    return {"status": rc, "tflops": t.value, "ms": ms.value}
 
 
 def sgemm_f32_release_workspace() -> tuple[int, int]:

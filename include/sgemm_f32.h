@@ -317,6 +317,19 @@ int sgemm_f32_status(int *status);
  * cudaError_t. */
 int sgemm_f32_wait_selftest(int *timed_out, float *seconds);
 
+/* FP32 pipe probe: the measured counterpart of the derived FP32 peak (SMs x 128 FP32 lanes
+ * x 2 FLOP x SM clock) that the GEMM kernels are held against. One kernel of SMs x 4 CTAs
+ * of 256 threads; each thread advances 16 independent register pairs `iters` times by
+ * packed FP32 multiply-adds (fma.rn.f32x2, the GEMM inner loop's instruction), with no
+ * memory traffic but one store that never happens. It runs once untimed, then `reps` times,
+ * each timed with CUDA events; synchronous, on a stream of its own.
+ *   iters          iterations per thread, 1 .. 2^24 (2^17 takes about 17 ms on GB300)
+ *   reps           timed launches, 1 .. 100
+ *   tflops         out: 4 x 16 x iters x threads FLOP / the median launch time, in TFLOP/s
+ *   ms_per_launch  out (may be NULL): that median time
+ * Returns 0, -1 (iters), -2 (reps), -3 (tflops NULL), or a cudaError_t. */
+int sgemm_f32_fma_probe(int iters, int reps, double *tflops, float *ms_per_launch);
+
 /* C = alpha * A * B + beta * C with A, B and C in HOST memory (row-major, the ld rules of
  * sgemm_f32). The product runs on the GPU in row blocks of about 2048 rows: B is copied to
  * the device once, and the copies of a block's A and C rows in and of its C rows out run on
