@@ -23,7 +23,8 @@ __all__ = [
     "sgemm_f32_3xtf32_workspace_size", "sgemm_f32_3xtf32_status", "sgemm_f32_ex_forced",
     "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
     "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm_f32_wait_selftest",
-    "sgemm_f32_release_workspace", "sgemm_f32_fma_probe", "sgemm", "EXPORTED",
+    "sgemm_f32_release_workspace", "sgemm_f32_fma_probe", "sgemm_f32_cluster_capacity",
+    "sgemm", "EXPORTED",
 ]
 
 # Every symbol include/sgemm_f32.h declares.
@@ -36,7 +37,7 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
             "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load",
             "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm_f32_release_workspace",
-            "sgemm_f32_fma_probe")
+            "sgemm_f32_fma_probe", "sgemm_f32_cluster_capacity")
 
 
 class SgemmError(RuntimeError):
@@ -78,6 +79,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_status.argtypes = [pi]
     L.sgemm_f32_wait_selftest.argtypes = [pi, ctypes.POINTER(ctypes.c_float)]
     L.sgemm_f32_release_workspace.argtypes = [psz]
+    L.sgemm_f32_cluster_capacity.argtypes = [i, i, pi]
     L.sgemm_f32_fma_probe.argtypes = [i, i, ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(ctypes.c_float)]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
@@ -253,6 +255,14 @@ def sgemm_f32_wait_selftest() -> dict:
     t, sec = ctypes.c_int(0), ctypes.c_float(0.0)
     rc = lib.sgemm_f32_wait_selftest(ctypes.byref(t), ctypes.byref(sec))
     return {"status": rc, "timed_out": t.value, "seconds": sec.value}
+
+
+def sgemm_f32_cluster_capacity(variant: int, cluster: int) -> tuple[int, int]:
+    """(call status, CTAs the device holds at once in clusters of `cluster`) for a
+    configuration, as the planner sees it (see the header)."""
+    n = ctypes.c_int(0)
+    rc = lib.sgemm_f32_cluster_capacity(variant, cluster, ctypes.byref(n))
+    return rc, n.value
 
 
 def sgemm_f32_fma_probe(iters: int = 1 << 17, reps: int = 5) -> dict:

@@ -611,6 +611,30 @@ int sgemm_f32_variant_info(int v, int *BM, int *BN, int *BK, int *threads, int *
   return built;
 }
 
+int sgemm_f32_cluster_capacity(int variant, int cluster, int *ctas) {
+  if (ctas) *ctas = 0;
+  if (variant < 0 || variant >= kNumVariants) return -1;
+  if (cluster < 1 || cluster > kMaxClusterSplit) return -2;
+  if (ctas == nullptr) return -3;
+  int num_sms = 0;
+  cudaError_t e = device_setup(&num_sms);
+  if (e != cudaSuccess) return (int)e;
+  const VariantShape &s = kVariants[variant];
+  if (s.thin >= 5) {  // cluster thin kernels: clusters of 1, 2, 4 or 8
+    if ((cluster & (cluster - 1)) != 0) return 0;
+    int t[4];
+    thin_cluster_capacity(t);
+    int l2 = 0;
+    while ((1 << l2) < cluster) ++l2;
+    *ctas = t[l2];
+    return 0;
+  }
+  const int *cap = cluster_capacity_table();
+  if (cap != nullptr && cluster >= 2 && variant_built(variant))
+    *ctas = cap[variant * (kMaxClusterSplit + 1) + cluster];
+  return 0;
+}
+
 const char *sgemm_f32_version(void) { return "sgemm_f32 0.1.0 sm_103a"; }
 
 int sgemm_f32_wait_selftest(int *timed_out, float *seconds) {

@@ -175,6 +175,18 @@ int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, 
 /* Tile configurations compiled into the library, for tests and tuning. */
 int sgemm_f32_num_variants(void);
 
+/* The cluster capacity the planner uses for configuration `variant` on the current device:
+ * *ctas = how many of its CTAs the device holds at once in thread-block clusters of
+ * `cluster` CTAs (the driver's cudaOccupancyMaxActiveClusters times the cluster size;
+ * clusters sit inside one GPC, so this can be below SMs x CTAs per SM). A split of every
+ * tile into `cluster` K slices is finished inside the cluster only when these CTAs fit in
+ * as few waves as unclustered ones. Configurations whose shared memory cannot hold a
+ * partial tile, and cluster sizes below 2, give 0; the cluster thin kernels (43, 44) give
+ * their capacity for clusters of 1, 2, 4 and 8 (0 for other sizes).
+ * Returns 0, -1 (variant out of range), -2 (cluster not in 1 .. 8), -3 (ctas NULL), or a
+ * cudaError_t of the device set-up. */
+int sgemm_f32_cluster_capacity(int variant, int cluster, int *ctas);
+
 /* Describe variant v: CTA tile BM x BN x BK, threads per CTA, per-thread TM x TN
  * accumulator tile, pipeline stages. Returns 0; 1 for a configuration that keeps its index
  * in the table but is not compiled into this build (the outputs are still filled; forcing
