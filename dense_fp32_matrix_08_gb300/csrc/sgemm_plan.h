@@ -101,7 +101,9 @@ constexpr VariantShape kVariants[] = {
     // A^T first, and the A tile arrives as [32 k][128 m] like the B tile. Their math loop
     // sustains ~9% more than 30 / 31 (measured 69.6 against 63.7 TFLOP/s at 8192^3).
     {128, 96, 32, 128, 8, 12, 2, 3, 1, smem_of(128, 96, 32, 2, 1), 1.06, true, false, true, false, 4, 0, true, 37},
-    {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 1.04, true, false, true, false, 5, 0, true, 38},
+    // 36 is forced-only: over 24 shapes from 200^3 to 3072^3 (every configuration and split
+    // measured per call on GB300) it was 2-40% slower than the better of 35 and 39 on each.
+    {128, 128, 32, 128, 8, 16, 3, 2, 1, smem_of(128, 128, 32, 3, 1), 1.04, false, false, true, false, 5, 0, true, 38},
     // 37, 38: the same two shapes reading A as stored and transposing each A tile in shared
     // memory (no workspace, no pre-pass; 128 x 128 with 2 stages to fit 2 CTAs/SM). They
     // are 3-5% slower than 35 / 36 at 8192^3 and 14-34% slower than the automatic choice
@@ -154,6 +156,11 @@ constexpr int kTmaVariant = 26;
 constexpr int kFirstKpairVariant = 27;
 constexpr int kThinMVariant = 33, kThinNVariant = 34;
 constexpr int kThinMaxDim = 64;  // thin kernels considered for M (thin-M) or N (thin-N) <= this
+// The cluster thin kernels (43, 44) are considered up to this M (thin-M) or N (thin-N):
+// where the streamed operand stays in L2 they beat the tiled kernels well past 64, e.g.
+// 5.1 against 6.0 us at 256^3, 6.5 against 10.1 at 384^3, 10.1 against 13.4 at
+// 1024 x 128 x 1024 (per call, measured on GB300); the model decides.
+constexpr int kThinClusterMaxDim = 1024;
 constexpr int kThinMKmax = 512, kThinNKmax = 2048;  // K slice bounds (shared memory)
 constexpr int kThinTmaVariant = 41, kThinTmaKmax = 1024;
 constexpr int kThinClusterVariant = 43;  // 43 thin-M, 44 thin-N
@@ -221,6 +228,10 @@ inline long long cluster_ctas(const Problem &p, int num_sms, int l2) {
 // kernels (thin 5, 6) take split = the cluster size (1, 2, 4 or 8), have no K bound and no
 // partial tiles, and fill HBM once about 85% of the SMs stream (a TMA streaming probe
 // reached the full copy bandwidth from 128 of 152 SMs).
+// A cluster thin kernel's K slices add their partial tiles through distributed shared
+// memory: two cluster barriers per wave (fitted with the GEMM kernels' fixed costs below).
+constexpr double kThinClusterSplitCycles = 1500.0;
+
 inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool beta_nz) {
   const VariantShape &s = kVariants[v];
   Plan pl;
@@ -273,6 +284,7 @@ inline Plan model_thin(const Problem &p, int v, int split, int num_sms, bool bet
   const double fill = cluster ? std::min(1.0, (double)ctas / (double)waves / (0.85 * num_sms))
                               : (double)ctas / (double)(waves * slots);
   pl.cycles = std::max(compute, bytes / (2800.0 * fill)) + 3000.0 * (double)waves +
+              (cluster && split > 1 ? kThinClusterSplitCycles * (double)waves : 0.0) +
               2000.0 * pl.launches;
   // The cluster kernels read both operands by TMA. A small operand whose rows TMA cannot
   // address (row stride not a multiple of 16 bytes, or a misaligned base) is first copied
@@ -354,6 +366,21 @@ inline int validate_colmajor(int transa, int transb, int m, int n, int k, int ld
 // The GEMM overlaps with streaming its algorithmic bytes at ~3400 bytes/cycle for the
 // chip. Split tiles add a reduction kernel afterwards: partials read, C read (beta != 0)
 // and written, plus ~2000 cycles of launch.
+// Fixed costs of the GEMM kernels' model, in SM cycles, fitted to per-call times measured
+// on GB300 (CUDA graphs of back-to-back calls, inputs from HBM) over 30 shapes from 200^3 to
+// 4096^3, thin and flat ones included, and every configuration and split of each: the
+// model's choice among the measured plans came within 0.7% of the fastest on 24 of them.
+// - kCtaFixedCycles: per CTA (whole tile or K slice): its start, first copies in flight
+//   and epilogue, which a short K loop does not amortise;
+// - kClusterFinishCycles: a split finished inside a cluster: its two cluster barriers,
+//   the distributed-shared-memory reads and the sparser placement of clusters (at 1024^3
+//   an 8-way cluster split and a 12-way split with the reduce kernel both take 50 us);
+// - kGemmLaunchCycles: the GEMM launch itself (the thin kernels' model charges the same
+//   kind of cost per launch).
+constexpr double kCtaFixedCycles = 9000.0;
+constexpr double kClusterFinishCycles = 12000.0;
+constexpr double kGemmLaunchCycles = 2000.0;
+
 inline Plan model_plan(const Problem &p, int v, long long main, int split, int num_sms,
                        bool beta_nz) {
   const VariantShape &s = kVariants[v];
@@ -373,9 +400,9 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   const long long tail = tiles - main;
   const long long slots = (long long)num_sms * s.min_blocks;
   const double rate = 128.0 * s.eff / s.min_blocks;  // FMA per cycle per resident CTA
-  const double t_full = (double)s.BM * s.BN * (double)(kt * s.BK) / rate + 2500.0;
-  const double t_slice = (double)s.BM * s.BN * (double)(kt_per * s.BK) / rate + 2500.0 +
-                         (double)s.BM * s.BN * 4.0 / (3400.0 / num_sms);
+  const double t_full = (double)s.BM * s.BN * (double)(kt * s.BK) / rate + kCtaFixedCycles;
+  const double t_slice = (double)s.BM * s.BN * (double)(kt_per * s.BK) / rate +
+                         kCtaFixedCycles + (double)s.BM * s.BN * 4.0 / (3400.0 / num_sms);
   // CTAs start in index order, `slots` at a time: whole tiles first, then slices. A round
   // with fewer CTAs than slots leaves some SMs with fewer resident CTAs, which then run
   // faster, though less than in proportion: n of min_blocks CTAs on an SM take about
@@ -451,7 +478,7 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
     // launch; two cluster barriers and each CTA reading one tile's worth over DSMEM
     pl.cluster = true;
     gemm_bytes -= part_bytes;
-    reduce = 1500.0 + (double)s.BM * s.BN * 4.0 / 64.0;
+    reduce = kClusterFinishCycles + (double)s.BM * s.BN * 4.0 / 64.0;
   }
   pl.main_tiles = (int)main;
   pl.split = split;
@@ -461,7 +488,7 @@ inline Plan model_plan(const Problem &p, int v, long long main, int split, int n
   pl.launches = (slices > 0 && !pl.cluster ? 2 : 1) + (pl.bt_bytes > 0 ? 1 : 0) +
                 (pl.pack_a || pl.at_a ? 1 : 0) + (pl.pack_b ? 1 : 0);
   pl.ws_bytes = pl.pre_bytes + (slices > 0 && !pl.cluster ? (size_t)part_bytes : 0);
-  pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce + bt_cycles;
+  pl.cycles = std::max(compute, gemm_bytes / 3400.0) + reduce + bt_cycles + kGemmLaunchCycles;
   if (main + slices > 0x7fffffffLL) {  // grid too large for one launch
     pl.ctas = 0;
     pl.cycles = std::numeric_limits<double>::infinity();
@@ -532,14 +559,16 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
     // 16-wide tiles exist for thin problems: the automatic plan keeps them for those, and
     // there prefers the TMA-fed thin kernels where they apply (measured 10-25% faster than
     // the copy-fed 16-wide tiles on 16 x 4096 x 4096 and 4096 x 16 x 8192)
-    if (force_v < 0 && ((s.BM <= 16 && p.M > kThinMaxDim) || (s.BN <= 16 && p.N > kThinMaxDim)))
+    if (force_v < 0 && s.thin < 5 &&
+        ((s.BM <= 16 && p.M > kThinMaxDim) || (s.BN <= 16 && p.N > kThinMaxDim)))
       continue;
     if (force_v < 0 && !s.thin && !s.tma && !s.kpair &&
         ((s.BM <= 16 && p.b_tma && !p.transa) || (s.BN <= 16 && p.a_tma && !p.transb)))
       continue;
     if (s.thin) {
       const bool thin_n_kind = s.thin == 2 || s.thin == 4 || s.thin == 6;
-      if (force_v < 0 && (thin_n_kind ? p.N : p.M) > kThinMaxDim) continue;
+      const int max_dim = s.thin >= 5 ? kThinClusterMaxDim : kThinMaxDim;
+      if (force_v < 0 && (thin_n_kind ? p.N : p.M) > max_dim) continue;
       if (s.thin == 3 && (!p.b_tma || p.transa)) continue;  // B read by TMA as stored
       if (s.thin == 4 && (!p.a_tma || p.transb)) continue;  // A read by TMA as stored
       if (s.thin >= 5) {  // cluster kernels: both operands read by TMA, the streamed one as

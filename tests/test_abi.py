@@ -158,11 +158,33 @@ def test_plan_thin_cluster_copies_an_unaligned_small_operand():
 
 
 def test_plan_small_cube_finishes_split_in_a_cluster():
-    """256^3 splits every tile along K: the slices run as one cluster and add their partial
-    tiles in shared memory, so the call is one launch with no workspace."""
+    """256^3 runs on the cluster thin kernel with every tile split along K: the slices run
+    as one cluster and add their partial tiles in shared memory, so the call is one launch
+    with no workspace (measured 5.15 us per call on GB300, against 6.1 for the tiled
+    kernel's cluster split)."""
     p = _plan(256, 256, 256, beta=0.0)
+    assert p["variant"] in THIN_CLUSTER
     assert p["split"] > 1 and p["main_tiles"] == 0
     assert p["launches"] == 1 and p["ws_bytes"] == 0
+
+
+def test_plan_recalibrated_choices():
+    """Choices of the model after its fixed costs were fitted to per-call times measured on
+    GB300 (48 shapes, every automatic configuration and split): small cubes and flat
+    products whose streamed operand stays in L2 take the cluster thin kernel, well past 64
+    rows (measured 6.55 against 10.1 us at 384^3, 10.0 against 13.3 at 128 x 1024 x 1024,
+    31.6 against 38.7 at 64 x 8192 x 1023); 128 x 4096 x 4096 splits 128 x 96 tiles 10 ways
+    with the reduce kernel (81 against 103 us for a 7-way cluster split); configuration 36
+    is never chosen."""
+    for shp in [(200, 200, 200), (384, 384, 384), (512, 512, 512), (128, 1024, 1024),
+                (64, 8192, 1023)]:
+        assert _plan(*shp, beta=0.5)["variant"] == 43, shp
+    p = _plan(128, 4096, 4096, beta=0.5)
+    assert p["variant"] == 35 and p["split"] == 10 and p["launches"] == 3
+    for n in (256, 512, 768, 1024, 1536, 2048, 3072, 4096, 8192):
+        assert _plan(n, n, n, beta=0.5)["variant"] != 36, n
+    for shp in [(2048, 2048, 256), (4096, 4096, 128), (1024, 8192, 1024)]:
+        assert _plan(*shp, beta=0.5)["variant"] != 36, shp
 
 
 def test_plan_calibration_points():
