@@ -630,9 +630,10 @@ def our_arm(args, dist: Dist):
         fp32["fp32_probe"] = {
             "tflops": probe["tflops"], "ms_per_launch": probe["ms"],
             "frac_of_derived_peak": probe["tflops"] / peak,
-            "what": "sgemm_f32_fma_probe: SMs x 4 CTAs x 256 threads, 16 independent "
-                    "fma.rn.f32x2 chains per thread, 2^17 iterations; median of 5 launches "
-                    "(CUDA events), run after the timed region"}
+            "what": "sgemm_f32_fma_probe: SMs x 8 CTAs x 256 threads, 8 independent "
+                    "fma.rn.f32x2 chains per thread on broadcast operand pairs, 2^17 "
+                    "iterations; median of 5 launches (CUDA events), run after the timed "
+                    "region"}
         fp32["frac_of_probe"] = achieved / probe["tflops"]
 
     # end to end: host buffers in pinned memory through the library's host-buffer entry

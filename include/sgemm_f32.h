@@ -330,14 +330,16 @@ int sgemm_f32_status(int *status);
 int sgemm_f32_wait_selftest(int *timed_out, float *seconds);
 
 /* FP32 pipe probe: the measured counterpart of the derived FP32 peak (SMs x 128 FP32 lanes
- * x 2 FLOP x SM clock) that the GEMM kernels are held against. One kernel of SMs x 4 CTAs
- * of 256 threads; each thread advances 16 independent register pairs `iters` times by
- * packed FP32 multiply-adds (fma.rn.f32x2, the GEMM inner loop's instruction), with no
- * memory traffic but one store that never happens. It runs once untimed, then `reps` times,
- * each timed with CUDA events; synchronous, on a stream of its own.
- *   iters          iterations per thread, 1 .. 2^24 (2^17 takes about 17 ms on GB300)
+ * x 2 FLOP x SM clock) that the GEMM kernels are held against. One kernel of SMs x 8 CTAs
+ * of 256 threads; each thread advances 8 independent register pairs `iters` times by
+ * packed FP32 multiply-adds (fma.rn.f32x2, the GEMM inner loop's instruction) whose
+ * multiplicands are pairs holding one value twice, with no memory traffic but one store
+ * that never happens. (With two different values in each multiplicand pair the pipe
+ * sustains about 12% less on GB300.) It runs once untimed, then `reps` times, each timed
+ * with CUDA events; synchronous, on a stream of its own.
+ *   iters          iterations per thread, 1 .. 2^24 (2^17 takes about 16 ms on GB300)
  *   reps           timed launches, 1 .. 100
- *   tflops         out: 4 x 16 x iters x threads FLOP / the median launch time, in TFLOP/s
+ *   tflops         out: 4 x 8 x iters x threads FLOP / the median launch time, in TFLOP/s
  *   ms_per_launch  out (may be NULL): that median time
  * Returns 0, -1 (iters), -2 (reps), -3 (tflops NULL), or a cudaError_t. */
 int sgemm_f32_fma_probe(int iters, int reps, double *tflops, float *ms_per_launch);
