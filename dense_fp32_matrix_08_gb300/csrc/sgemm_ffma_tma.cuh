@@ -220,15 +220,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
           b2[2 * jj] = pack2(fbc[jj].x, fbc[jj].y);
           b2[2 * jj + 1] = pack2(fbc[jj].z, fbc[jj].w);
         }
+        unsigned long long a2[TM];
 #pragma unroll
         for (int i = 0; i < TM; ++i) {
           const float4 &f = fac[i >> 2];
           const int e = i & 3;
           const float a = e == 0 ? f.x : e == 1 ? f.y : e == 2 ? f.z : f.w;
-          const unsigned long long a2 = pack2(a, a);
-#pragma unroll
-          for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], a2, b2[j]);
+          a2[i] = pack2(a, a);
         }
+        // j outer: each B pair feeds TM consecutive instructions
+#pragma unroll
+        for (int j = 0; j < TN / 2; ++j)
+#pragma unroll
+          for (int i = 0; i < TM; ++i) ffma2(acc[i][j], a2[i], b2[j]);
       }
     } else {
       // Fragments are double-buffered: the A float4s of chunk c + 1 (4 k each) load while
