@@ -24,6 +24,7 @@ __all__ = [
     "sgemm_f32_autotune", "sgemm_f32_tune_count", "sgemm_f32_tune_clear", "sgemm_f32_tune_save",
     "sgemm_f32_tune_load", "sgemm_f32_host", "sgemm_f32_wait_selftest",
     "sgemm_f32_release_workspace", "sgemm_f32_fma_probe", "sgemm_f32_cluster_capacity",
+    "sgemm_f32_workspace_size_min",
     "sgemm", "EXPORTED",
 ]
 
@@ -37,7 +38,8 @@ EXPORTED = ("sgemm_f32", "sgemm_f32_ws", "sgemm_f32_forced", "sgemm_f32_workspac
             "sgemm_f32_ex_forced", "sgemm_f32_autotune", "sgemm_f32_tune_count",
             "sgemm_f32_tune_clear", "sgemm_f32_tune_save", "sgemm_f32_tune_load",
             "sgemm_f32_host", "sgemm_f32_wait_selftest", "sgemm_f32_release_workspace",
-            "sgemm_f32_fma_probe", "sgemm_f32_cluster_capacity")
+            "sgemm_f32_fma_probe", "sgemm_f32_cluster_capacity",
+            "sgemm_f32_workspace_size_min")
 
 
 class SgemmError(RuntimeError):
@@ -83,6 +85,7 @@ def _load() -> ctypes.CDLL:
     L.sgemm_f32_fma_probe.argtypes = [i, i, ctypes.POINTER(ctypes.c_double),
                                       ctypes.POINTER(ctypes.c_float)]
     L.sgemm_f32_workspace_size.argtypes = [i, i, i, i, i, i, psz]
+    L.sgemm_f32_workspace_size_min.argtypes = [i, i, i, i, i, i, psz]
     L.sgemm_f32_plan.argtypes = [i, i, i, i, i, i, f, f, i, pi, pi, pi, pi, psz]
     L.sgemm_f32_num_variants.argtypes = []
     L.sgemm_f32_variant_info.argtypes = [i] + [pi] * 7
@@ -291,6 +294,14 @@ def sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc) -> tuple[int, int]:
     """(status, bytes)."""
     b = ctypes.c_size_t(0)
     rc = lib.sgemm_f32_workspace_size(M, N, K, lda, ldb, ldc, ctypes.byref(b))
+    return rc, b.value
+
+
+def sgemm_f32_workspace_size_min(M, N, K, lda, ldb, ldc) -> tuple[int, int]:
+    """(status, bytes): the smallest workspace sgemm_f32_ws runs this problem with (the plan
+    without its A^T copy; see the header)."""
+    b = ctypes.c_size_t(0)
+    rc = lib.sgemm_f32_workspace_size_min(M, N, K, lda, ldb, ldc, ctypes.byref(b))
     return rc, b.value
 
 

@@ -564,6 +564,28 @@ int sgemm_f32_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
                         nullptr, bytes);
 }
 
+int sgemm_f32_workspace_size_min(int M, int N, int K, int lda, int ldb, int ldc,
+                                 size_t *bytes) {
+  if (bytes) *bytes = 0;
+  Problem pr{M, N, K, lda, ldb, ldc};
+  pr.tma_ok = lda % 4 == 0 && ldb % 4 == 0;  // pointers assumed 16-byte aligned
+  pr.kpair_ok = lda % 4 == 0;
+  pr.a_tma = lda % 4 == 0;
+  pr.b_tma = ldb % 4 == 0;
+  int rc = validate(pr, 1.0f, true, true, true);
+  if (rc != 0) return rc;
+  if (M == 0 || N == 0) return 0;
+  int num_sms = 0;
+  cudaError_t e = device_setup(&num_sms);
+  if (e != cudaSuccess) return (int)e;
+  thin_cluster_capacity(pr.cluster_ctas);
+  pr.cluster_cap = cluster_capacity_table();
+  // the plan sgemm_f32_ws makes when the workspace cannot hold the A^T copy
+  const Plan pl = without_at_copy(pr, automatic_plan(pr, 1.0f, 1.0f, num_sms));
+  if (bytes) *bytes = pl.ws_bytes;
+  return 0;
+}
+
 int sgemm_f32_plan(int M, int N, int K, int lda, int ldb, int ldc, float alpha, float beta,
                    int num_sms, int *variant, int *split, int *main_tiles, int *launches,
                    size_t *ws_bytes) {

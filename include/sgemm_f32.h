@@ -40,7 +40,9 @@
  *   call does not map memory again; it holds the largest workspace a call has needed (more
  *   when calls on several streams overlap) until sgemm_f32_release_workspace() returns it
  *   or the process exits. sgemm_f32_workspace_size() reports the size a call needs;
- *   sgemm_f32_ws() takes a caller-provided workspace instead.
+ *   sgemm_f32_ws() takes a caller-provided workspace instead, and with
+ *   sgemm_f32_workspace_size_min() bytes it needs no A^T copy: it then holds split-K
+ *   partial tiles only (and aligned copies of operands TMA cannot address).
  *
  * Asynchrony
  *   Every compute call enqueues its kernels on `stream` (0 = the legacy default stream) and
@@ -138,11 +140,25 @@ int sgemv_f32(int trans, int M, int N, float alpha, const float *A, int lda, con
 int sdot_f32(int n, const float *x, int incx, const float *y, int incy, float *result,
              cudaStream_t stream);
 
-/* Bytes of split-K workspace that sgemm_f32 would allocate for this problem on the
- * current device (0 when the chosen plan needs none). Host-only query. Returns the same
- * negative codes as sgemm_f32 for illegal shapes or leading dimensions, else 0. */
+/* Bytes of workspace that sgemm_f32 would allocate for this problem on the current device
+ * (0 when the chosen plan needs none): the pre-pass copies (A^T for the k-major plans,
+ * aligned operand copies) and the split-K partial tiles, for beta != 0 (a beta = 0 call
+ * may plan differently: sgemm_f32_plan reports its plan). Pointers are assumed 16-byte
+ * aligned. Host-side query (the first call sets up the device). Returns the same negative
+ * codes as sgemm_f32 for illegal shapes or leading dimensions, else 0 or a cudaError_t. */
 int sgemm_f32_workspace_size(int M, int N, int K, int lda, int ldb, int ldc,
                              size_t *bytes);
+
+/* The smallest workspace with which sgemm_f32_ws runs this problem: the same plan without
+ * its A^T copy, i.e. only the split-K partial tiles (and aligned copies of operands that
+ * TMA cannot address). Given a workspace of at least this size but smaller than
+ * sgemm_f32_workspace_size, sgemm_f32_ws runs the twin configuration, which transposes A
+ * in shared memory: the same tiles, K slices and k order, so the result is bitwise the
+ * same, with one launch fewer and no A^T copy. (At 8192^3 on GB300: 21 MiB instead of
+ * 290 MB, at 70.7 against 74.7 TFLOP/s.) Equal to sgemm_f32_workspace_size for plans
+ * without an A^T copy. Same conventions and return codes as sgemm_f32_workspace_size. */
+int sgemm_f32_workspace_size_min(int M, int N, int K, int lda, int ldb, int ldc,
+                                 size_t *bytes);
 
 /* Same as sgemm_f32, but any split-K workspace comes from the caller: `workspace` is a
  * device buffer of `workspace_bytes` bytes, 16-byte aligned, not read before it is written

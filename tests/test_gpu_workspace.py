@@ -56,3 +56,42 @@ def test_release_with_nothing_held():
     assert sg.sgemm_f32_release_workspace()[0] == 0
     rc, released = sg.sgemm_f32_release_workspace()
     assert rc == 0 and released == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(4096, 4096, 4096), (2100, 2600, 300), (16, 4096, 4096)])
+def test_minimal_workspace_runs_the_twin(M, N, K):
+    """sgemm_f32_ws with the workspace sgemm_f32_workspace_size_min reports: the plan
+    without its A^T copy (split-K partial tiles only), run by the twin configuration that
+    transposes A in shared memory, bitwise the same as sgemm_f32; one byte less is refused
+    (-13) without touching C. Plans without an A^T copy need the same size either way."""
+    import dense_fp32_matrix_08_gb300 as sg
+
+    rc, full = sg.sgemm_f32_workspace_size(M, N, K, K, N, N)
+    assert rc == 0
+    rc, small = sg.sgemm_f32_workspace_size_min(M, N, K, K, N, N)
+    assert rc == 0 and small <= full
+    plan = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, 1.0, 0)
+    if plan["variant"] in (35, 36, 39, 40):
+        at_copy = -(-4 * K * (-(-M // 4) * 4) // 256) * 256
+        assert full - small == at_copy
+    else:
+        assert small == full
+    A, B, C = make_inputs(M, N, K, seed=M + 7)
+    dA, dB = A.cuda(), B.cuda()
+    ref = C.cuda()
+    assert sg.sgemm_f32(M, N, K, 1.0, dA, K, dB, N, 1.0, ref, N) == 0
+    ws = torch.empty(max(small, 16), dtype=torch.uint8, device="cuda")
+    out = C.cuda()
+    assert sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, out, N, ws.data_ptr(), small) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(out, ref)
+    if small > 0:
+        before = C.cuda()
+        rc = sg.sgemm_f32_ws(M, N, K, 1.0, dA, K, dB, N, 1.0, before, N, ws.data_ptr(),
+                             small - 1)
+        torch.cuda.synchronize()
+        assert rc == -13
+        assert torch.equal(before.cpu(), C)
+    rows = np.array([0, M // 2, M - 1])
+    R, S = oracle.sgemm_f64_rows(A, B, C, 1.0, 1.0, rows)
+    assert_bound(out.cpu().numpy()[rows], R, S, 1.0, C.numpy()[rows], "minimal workspace")
