@@ -251,6 +251,29 @@ def max_sm_clock_mhz() -> float:
         return 2070.0  # GB300 maximum SM clock
 
 
+def host_link_gbs(h: torch.Tensor, stream) -> dict:
+    """Plain copy rates between the pinned host tensor `h` and the device, measured right
+    after the end-to-end leg (5 copies each way, CUDA events): the host link the e2e
+    figure depends on, which differs between machines and with the host's other load."""
+    d = torch.empty_like(h, device="cuda")
+    n = h.numel() * h.element_size()
+    out = {}
+    with torch.cuda.stream(stream):
+        for name, dst, src in (("h2d_GBs", d, h), ("d2h_GBs", h, d)):
+            dst.copy_(src, non_blocking=True)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(5):
+                dst.copy_(src, non_blocking=True)
+            e1.record(stream)
+            e1.synchronize()
+            out[name] = round(5 * n / (e0.elapsed_time(e1) * 1e-3) / 1e9, 1)
+    del d
+    out["bytes_per_copy"] = n
+    return out
+
+
 def cpu_model() -> str:
     """The host CPU's model name (lscpu), for the CPU baseline's record."""
     try:
@@ -664,7 +687,7 @@ def our_arm(args, dist: Dist):
                "unit": UNIT, "api": "sgemm_f32_host (pinned host buffers)",
                "h2d_bytes_per_step": 4 * (M * K + K * N + M * N),
                "d2h_bytes_per_step": 4 * M * N, "ms_per_step": 1e3 * e2e_t / args.e2e_steps,
-               "parity": e2e_parity}
+               "parity": e2e_parity, "host_link": host_link_gbs(hC, stream)}
 
     secondary = {}
     if not args.no_secondary and w.name == HEADLINE.name:
