@@ -408,14 +408,26 @@ def tensor_core_variant(sg, args, stream, w, dA, dB, dC, C0):
                                  "the time includes the hi/lo split passes"}}
 
 
-def time_steps(fn, steps, stream):
+def time_steps(fn, steps, stream, per_step=None):
+    """Seconds for `steps` calls of fn enqueued back to back on `stream` (CUDA events on
+    both sides). With a list `per_step`, an event after every call also gives each step's
+    milliseconds (no synchronisation in between, so the total is unchanged)."""
     start = torch.cuda.Event(enable_timing=True)
-    end = torch.cuda.Event(enable_timing=True)
+    marks = []
     start.record(stream)
     for _ in range(steps):
         fn()
+        if per_step is not None:
+            marks.append(torch.cuda.Event(enable_timing=True))
+            marks[-1].record(stream)
+    end = torch.cuda.Event(enable_timing=True)
     end.record(stream)
     end.synchronize()
+    if per_step is not None:
+        prev = start
+        for m in marks:
+            per_step.append(round(prev.elapsed_time(m), 3))
+            prev = m
     return start.elapsed_time(end) / 1e3
 
 
@@ -681,13 +693,15 @@ def our_arm(args, dist: Dist):
             e2e_step()
             stream.synchronize()
             dist.barrier()
-            e2e_t = time_steps(e2e_step, args.e2e_steps, stream)
+            e2e_steps_ms = []
+            e2e_t = time_steps(e2e_step, args.e2e_steps, stream, e2e_steps_ms)
         e2e_t = dist.max(e2e_t)
         e2e = {"value": replica_throughput(flops, args.e2e_steps, dist.world, e2e_t),
                "unit": UNIT, "api": "sgemm_f32_host (pinned host buffers)",
                "h2d_bytes_per_step": 4 * (M * K + K * N + M * N),
                "d2h_bytes_per_step": 4 * M * N, "ms_per_step": 1e3 * e2e_t / args.e2e_steps,
-               "parity": e2e_parity, "host_link": host_link_gbs(hC, stream)}
+               "parity": e2e_parity, "host_link": host_link_gbs(hC, stream),
+               "step_ms": e2e_steps_ms}
 
     secondary = {}
     if not args.no_secondary and w.name == HEADLINE.name:
