@@ -131,7 +131,7 @@ constexpr VariantShape kVariants[] = {
     {128, 16, 8, 512, 4, 16, 2, 1, 1, 0, 0.8, true, false, false, false, 0, 6},
     // 45: 39's twin, transposing each A tile in shared memory (3 CTAs/SM; forced-only, and
     // the substitute for 39 when a caller workspace cannot hold the A^T copy)
-    {128, 64, 32, 128, 8, 8, 2, 3, 1, smem_of(128, 64, 32, 2, 1) + 16384, 0.98, false, false, true, false, 10},
+    {128, 64, 32, 128, 8, 8, 2, 3, 1, smem_of(128, 64, 32, 2, 1) + 16384, 0.98, true, false, true, false, 10},
 };
 constexpr int kNumVariants = sizeof(kVariants) / sizeof(kVariants[0]);
 
@@ -152,6 +152,17 @@ constexpr bool retired_are_forced_only() {
   return true;
 }
 static_assert(retired_are_forced_only(), "only forced-only copy-fed configurations retire");
+// Whether configuration v is the shared-memory-transpose twin of a k-major one.
+constexpr bool is_transpose_twin(int v) {
+  for (int u = 0; u < kNumVariants; ++u)
+    if (kVariants[u].twin == v) return true;
+  return false;
+}
+// The automatic plan takes a transpose twin only for K loops of at least this many K
+// blocks: its per-block transpose and its fewer CTAs per SM do not pay on shorter ones
+// (measured 9-10% behind configurations 32 / 39 at 2 and 4 K blocks, ahead at 8 and more).
+constexpr int kTwinMinKBlocks = 8;
+
 constexpr int kTmaVariant = 26;
 constexpr int kFirstKpairVariant = 27;
 constexpr int kThinMVariant = 33, kThinNVariant = 34;
@@ -556,6 +567,7 @@ inline Plan make_plan(const Problem &p, float alpha, float beta, int num_sms, in
       continue;
     if (kVariants[v].kpair && (!p.kpair_ok || (force_v < 0 && !p.b_kmajor))) continue;
     const VariantShape &s = kVariants[v];
+    if (force_v < 0 && is_transpose_twin(v) && ceil_div(p.K, s.BK) < kTwinMinKBlocks) continue;
     // 16-wide tiles exist for thin problems: the automatic plan keeps them for those, and
     // there prefers the TMA-fed thin kernels where they apply (measured 10-25% faster than
     // the copy-fed 16-wide tiles on 16 x 4096 x 4096 and 4096 x 16 x 8192)

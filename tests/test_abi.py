@@ -110,6 +110,18 @@ def test_shared_memory_transpose_twins_are_not_automatic():
         assert _plan(*shp, beta=0.5)["variant"] not in (37, 38), shp
 
 
+def test_plan_transpose_twin_45_for_long_k():
+    """Configuration 45 (configuration 39's tiles with A transposed in the CTA, so no A^T
+    copy) is automatic for K loops of 8 or more K blocks, where it measured fastest on GB300
+    (4096 x 256 x 4096: 147.9 against 174.4 us per call; 2048^3: 264.7 against 273.3).
+    Below that its per-block transpose and its 3 CTAs per SM do not pay (2432 x 2432 x 64:
+    30.8 against 27.6 us), and the plan takes another configuration."""
+    for shp in [(4096, 256, 4096), (2048, 2048, 2048), (256, 256, 8192)]:
+        assert _plan(*shp, beta=0.5)["variant"] == 45, shp
+    for shp in [(2432, 2432, 64), (4096, 4096, 128)]:
+        assert _plan(*shp, beta=0.5)["variant"] != 45, shp
+
+
 def _plan(M, N, K, beta=1.0):
     p = sg.sgemm_f32_plan(M, N, K, K, N, N, 1.0, beta, SMS)
     assert p["status"] == 0
