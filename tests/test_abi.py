@@ -67,6 +67,30 @@ def test_null_ab_allowed_when_not_read():
     assert p["launches"] == 0
 
 
+def test_query_entry_points_reject_illegal_arguments_before_cuda():
+    # the workspace queries return sgemm_f32's codes (argument positions of sgemm_f32)
+    for f in (sg.sgemm_f32_workspace_size, sg.sgemm_f32_workspace_size_min):
+        assert f(-1, 4, 4, 4, 4, 4) == (-1, 0)
+        assert f(4, 4, 4, 3, 4, 4) == (-6, 0)   # lda < K
+        assert f(4, 4, 4, 4, 3, 4) == (-8, 0)   # ldb < N
+        assert f(4, 4, 4, 4, 4, 3) == (-11, 0)  # ldc < N
+    # an empty problem needs no workspace; this query answers before any device set-up
+    assert sg.sgemm_f32_workspace_size_min(0, 4, 4, 4, 4, 4) == (0, 0)
+    # FP32 pipe probe: iters in 1 .. 2^24, reps in 1 .. 100, tflops not NULL
+    for iters, reps, code in ((0, 5, -1), ((1 << 24) + 1, 5, -1), (16, 0, -2), (16, 101, -2)):
+        r = sg.sgemm_f32_fma_probe(iters, reps)
+        assert r == {"status": code, "tflops": 0.0, "ms": 0.0}
+    lib = ctypes.CDLL(sg.LIB_PATH)
+    assert lib.sgemm_f32_fma_probe(16, 5, None, None) == -3
+    # cluster capacity: variant in range, cluster in 1 .. 8, ctas not NULL
+    n = sg.sgemm_f32_num_variants()
+    assert sg.sgemm_f32_cluster_capacity(-1, 2) == (-1, 0)
+    assert sg.sgemm_f32_cluster_capacity(n, 2) == (-1, 0)
+    assert sg.sgemm_f32_cluster_capacity(0, 0) == (-2, 0)
+    assert sg.sgemm_f32_cluster_capacity(0, 9) == (-2, 0)
+    assert lib.sgemm_f32_cluster_capacity(0, 2, None) == -3
+
+
 def test_forced_variant_out_of_range():
     n = sg.sgemm_f32_num_variants()
     assert sg.sgemm_f32_forced(4, 4, 4, 1.0, 8, 4, 8, 4, 0.0, 8, 4, n, 1, stream=0) == -14
