@@ -408,6 +408,50 @@ def tensor_core_variant(sg, args, stream, w, dA, dB, dC, C0):
                                  "the time includes the hi/lo split passes"}}
 
 
+def minimal_workspace_variant(sg, args, stream, w, dA, dB, dC, C0, plan):
+    """The same product through sgemm_f32_ws given only the smallest workspace it runs with
+    (sgemm_f32_workspace_size_min: the split-K partial tiles, no A^T copy). The plan is the
+    default one with A transposed in shared memory by the same kernel's twin configuration,
+    so the result must be bitwise the default call's, which this leg checks once."""
+    M, N, K = w.M, w.N, w.K
+    s_handle = stream.cuda_stream
+    rc, nbytes = sg.sgemm_f32_workspace_size_min(M, N, K, K, N, N)
+    if rc != 0:
+        raise RuntimeError(f"sgemm_f32_workspace_size_min returned {rc}")
+    ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dC.device)
+
+    def step():
+        rc = sg.lib.sgemm_f32_ws(M, N, K, w.alpha, dA.data_ptr(), K, dB.data_ptr(), N,
+                                 w.beta, dC.data_ptr(), N, ws.data_ptr(), nbytes, s_handle)
+        if rc != 0:
+            raise RuntimeError(f"sgemm_f32_ws returned {rc}")
+
+    ref = C0.to(dC.device)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        rc = sg.lib.sgemm_f32(M, N, K, w.alpha, dA.data_ptr(), K, dB.data_ptr(), N, w.beta,
+                              ref.data_ptr(), N, s_handle)
+        if rc != 0:
+            raise RuntimeError(f"sgemm_f32 returned {rc}")
+        dC.copy_(C0)
+        step()
+    stream.synchronize()
+    bitwise = bool(torch.equal(dC, ref))
+    del ref
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+        t = time_steps(step, args.steps, stream)
+    rc, status = sg.sgemm_f32_status()
+    value = w.flops * args.steps / t / 1e12
+    with_copy = plan["ws_bytes"] is not None and nbytes < plan["ws_bytes"]
+    return {"value": value, "unit": UNIT, "ms_per_step": 1e3 * t / args.steps,
+            "api": "sgemm_f32_ws with sgemm_f32_workspace_size_min bytes",
+            "ws_bytes": nbytes, "default_ws_bytes": plan["ws_bytes"],
+            "launches_per_step": plan["launches"] - 1 if with_copy else plan["launches"],
+            "bitwise_equal_to_default": bitwise, "device_status": status}
+
+
 def time_steps(fn, steps, stream, per_step=None):
     """Seconds for `steps` calls of fn enqueued back to back on `stream` (CUDA events on
     both sides). With a list `per_step`, an event after every call also gives each step's
@@ -712,6 +756,9 @@ def our_arm(args, dist: Dist):
     variants = {}
     if not args.no_variants:
         variants["3xtf32_tensor_core"] = tensor_core_variant(sg, args, stream, w, dA, dB, dC, C0)
+        if not forced:
+            variants["minimal_workspace"] = minimal_workspace_variant(sg, args, stream, w, dA,
+                                                                      dB, dC, C0, plan)
 
     if dist.rank == 0:
         line = {
