@@ -25,25 +25,35 @@ namespace sgemm {
 namespace {
 
 struct CopyStreams {
-  std::once_flag once;
-  cudaStream_t in = nullptr, out = nullptr;
-  cudaError_t err = cudaSuccess;
+  std::mutex mu;
+  cudaStream_t in = nullptr, out = nullptr;  // set together, once both exist
 };
 CopyStreams g_copy[64];
 
+// The current device's two copy streams, created by the first call on the device that
+// succeeds and kept until exit. A failed creation is returned and tried again by the next
+// call, not kept for the process.
 cudaError_t copy_streams(cudaStream_t *in, cudaStream_t *out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   CopyStreams &c = g_copy[dev];
-  std::call_once(c.once, [&c]() {
-    c.err = cudaStreamCreateWithFlags(&c.in, cudaStreamNonBlocking);
-    if (c.err == cudaSuccess) c.err = cudaStreamCreateWithFlags(&c.out, cudaStreamNonBlocking);
-  });
+  std::lock_guard<std::mutex> lock(c.mu);
+  if (c.in == nullptr) {
+    cudaStream_t si = nullptr, so = nullptr;
+    e = cudaStreamCreateWithFlags(&si, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&so, cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      if (si != nullptr) cudaStreamDestroy(si);
+      return e;
+    }
+    c.in = si;
+    c.out = so;
+  }
   *in = c.in;
   *out = c.out;
-  return c.err;
+  return cudaSuccess;
 }
 
 // Events of one call; destroyed after enqueueing (CUDA releases them once complete).
@@ -153,11 +163,19 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
     if (e == cudaSuccess) e = cudaEventRecord(ev_in[i], s_in);
   };
 
-  std::vector<int> kb{0};  // chunk boundaries: a first chunk of 256, then about K / 8
+  // Chunk boundaries: a first chunk of 256, then each chunk twice as long as the one before
+  // (from the second chunk on, the copies run ahead of the GEMMs); a rest shorter than half
+  // a chunk joins that chunk. K = 8192 gives 256, 512, 1024, 2048 and 4352.
+  std::vector<int> kb{0};
   if (chunk_head) {
-    const int kc = (int)std::min<long long>(K, ceil_div(ceil_div(K, 8), 128) * 128);
     kb.push_back(std::min(K, 256));
-    while (kb.back() < K) kb.push_back(std::min(K, kb.back() + kc));
+    long long len = 256;
+    while (kb.back() < K) {
+      len *= 2;
+      long long next = kb.back() + len;
+      if (K - next < len / 2) next = K;
+      kb.push_back((int)std::min<long long>(K, next));
+    }
   } else {
     kb.push_back(K);
   }

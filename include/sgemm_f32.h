@@ -365,13 +365,13 @@ int sgemm_f32_fma_probe(int iters, int reps, double *tflops, float *ms_per_launc
  * the device once, and the copies of a block's A and C rows in and of its C rows out run on
  * two library-owned copy streams that overlap the GEMMs of the neighbouring blocks, which
  * run on `stream`. With two or more blocks, K >= 1024 and B of 32 MB or more, the first
- * block is computed in K chunks (256, then about K / 8) as B and its A rows arrive: each
- * chunk's alpha * A B is added into the block, and beta * C (copied in behind the chunks)
- * is added last, so the GEMMs start after the first small chunk. That block's result is
- * rounded to FP32 once per chunk and is not bitwise the single-call result (it meets the
- * same error bound). Device buffers come from the library's workspace pool (B, two A-block
- * and C-block buffers, and for that head with beta != 0 one more C-block buffer) and are
- * released in stream order.
+ * block is computed in K chunks (256, then each twice the one before) as B and its A rows
+ * arrive: each chunk's alpha * A B is added into the block, and beta * C (copied in behind
+ * the chunks) is added last, so the GEMMs start after the first small chunk. That block's
+ * result is rounded to FP32 once per chunk and is not bitwise the single-call result (it
+ * meets the same error bound). Device buffers come from the library's workspace pool (B,
+ * two A-block and C-block buffers, and for that head with beta != 0 one more C-block
+ * buffer) and are released in stream order.
  * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
  * overlap; pageable memory works, with copies that do not overlap.
  * Asynchronous on `stream`: C on the host is final once `stream` has been synchronised;
