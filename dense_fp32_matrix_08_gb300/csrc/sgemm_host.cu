@@ -7,7 +7,8 @@
 //   copy-out stream                               C0 out    C1 out   ...
 //
 // With a large B the first block is computed in K chunks as B and A0 arrive (see below), so
-// the GEMMs start after one chunk instead of all of B.
+// the GEMMs start after one chunk instead of all of B. The last block is computed in two row
+// parts, so that only the second part's copy out follows the last GEMM.
 //
 // Device buffers (B whole; A and C blocks, double-buffered) come from the library's
 // workspace pool on the caller's stream and go back to it when the work is done.
@@ -149,6 +150,14 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_start, 0);
 
   auto rows_of = [&](int i) { return std::min(mb, M - i * mb); };
+  // Tail: when there are two or more blocks, the last one (if 1024 rows or more) is computed
+  // in two parts, its last 3/8 (rounded up to 128 rows) apart, so that only their copy out
+  // follows the last GEMM. 2048 rows split as 1280 + 768.
+  auto tail_rows = [&](int rows) -> int {
+    if (blocks < 2 || rows < 1024) return 0;
+    const long long t = ceil_div(3LL * rows, 8 * 128) * 128;
+    return t < rows ? (int)t : 0;
+  };
   std::vector<cudaEvent_t> ev_in(blocks, nullptr), ev_done(blocks, nullptr),
       ev_out(blocks, nullptr);
   auto copy_in = [&](int i) {  // on s_in: A and C rows of block i into buffer i % 2
@@ -209,8 +218,18 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
     copy_in(0);
   }
   if (blocks > 1) copy_in(1);
+  // on s_out, once `ready` has completed: rows [p0, p0 + n) of block i back to the host
+  auto copy_out = [&](int i, int p0, int n, cudaEvent_t ready) {
+    cudaError_t r = cudaStreamWaitEvent(s_out, ready, 0);
+    if (r == cudaSuccess)
+      r = cudaMemcpy2DAsync(C + (long long)(i * mb + p0) * ldc, (size_t)ldc * 4,
+                            dC[i % 2] + (size_t)p0 * N, (size_t)N * 4, (size_t)N * 4, n,
+                            cudaMemcpyDeviceToHost, s_out);
+    return r;
+  };
   for (int i = 0; i < blocks && e == cudaSuccess; ++i) {
-    const int r0 = i * mb, rows = rows_of(i);
+    const int rows = rows_of(i);
+    int out0 = 0;  // first row of the block still to be copied out after its GEMMs
     if (i == 0 && chunk_head) {
       for (int c = 0; c < nchunks && e == cudaSuccess && rc == 0; ++c) {
         const int k0 = kb[c], kn = kb[c + 1] - kb[c];
@@ -231,17 +250,27 @@ extern "C" int sgemm_f32_host(int M, int N, int K, float alpha, const float *A, 
     } else {
       e = cudaStreamWaitEvent(stream, ev_in[i], 0);
       if (e != cudaSuccess) break;
-      // the block's product on the caller's stream, through the library's own entry point
-      rc = sgemm_f32(rows, N, K, alpha, reads_ab ? dA[i % 2] : nullptr, std::max(1, K),
-                     reads_ab ? dB : nullptr, N, beta, dC[i % 2], N, stream);
-      if (rc != 0) break;
+      // The block's product on the caller's stream, through the library's own entry point.
+      // The last block's first rows go out while the GEMM of its tail runs.
+      const int part = i == blocks - 1 ? rows - tail_rows(rows) : rows;
+      for (int p0 = 0; p0 < rows && e == cudaSuccess && rc == 0; p0 += part) {
+        const int n = std::min(part, rows - p0);
+        rc = sgemm_f32(n, N, K, alpha, reads_ab ? dA[i % 2] + (size_t)p0 * K : nullptr,
+                       std::max(1, K), reads_ab ? dB : nullptr, N, beta,
+                       dC[i % 2] + (size_t)p0 * N, N, stream);
+        if (rc == 0 && p0 + n < rows) {
+          cudaEvent_t ev_part = nullptr;
+          e = evs.make(&ev_part);
+          if (e == cudaSuccess) e = cudaEventRecord(ev_part, stream);
+          if (e == cudaSuccess) e = copy_out(i, p0, n, ev_part);
+        }
+        out0 = p0;
+      }
+      if (e != cudaSuccess || rc != 0) break;
     }
     e = evs.make(&ev_done[i]);
     if (e == cudaSuccess) e = cudaEventRecord(ev_done[i], stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s_out, ev_done[i], 0);
-    if (e == cudaSuccess)
-      e = cudaMemcpy2DAsync(C + (long long)r0 * ldc, (size_t)ldc * 4, dC[i % 2], (size_t)N * 4,
-                            (size_t)N * 4, rows, cudaMemcpyDeviceToHost, s_out);
+    if (e == cudaSuccess) e = copy_out(i, out0, rows - out0, ev_done[i]);
     if (e == cudaSuccess) e = evs.make(&ev_out[i]);
     if (e == cudaSuccess) e = cudaEventRecord(ev_out[i], s_out);
     // block i + 2 reuses buffer i % 2 once block i's result has left it

@@ -369,9 +369,11 @@ int sgemm_f32_fma_probe(int iters, int reps, double *tflops, float *ms_per_launc
  * arrive: each chunk's alpha * A B is added into the block, and beta * C (copied in behind
  * the chunks) is added last, so the GEMMs start after the first small chunk. That block's
  * result is rounded to FP32 once per chunk and is not bitwise the single-call result (it
- * meets the same error bound). Device buffers come from the library's workspace pool (B,
- * two A-block and C-block buffers, and for that head with beta != 0 one more C-block
- * buffer) and are released in stream order.
+ * meets the same error bound). With two or more blocks, the last block, if 1024 rows or
+ * more, is computed in two calls, its last 3/8 (rounded up to 128 rows) apart, and the
+ * first part's rows go back while the second part computes. Device buffers come from the
+ * library's workspace pool (B, two A-block and C-block buffers, and for that head with
+ * beta != 0 one more C-block buffer) and are released in stream order.
  * Host memory should be page-locked (cudaHostAlloc / cudaHostRegister) for the copies to
  * overlap; pageable memory works, with copies that do not overlap.
  * Asynchronous on `stream`: C on the host is final once `stream` has been synchronised;

@@ -27,8 +27,26 @@ def _host_view(x: torch.Tensor, ld: int, pinned: bool) -> torch.Tensor:
     return buf, view
 
 
+def _block_edges(M):
+    """First rows of the row blocks and of the last block's separately computed tail, by the
+    rule sgemm_f32_host documents: about 2048 rows a block (a multiple of 128, at most 8
+    blocks); with two or more blocks, the last block's last 3/8 (rounded up to 128 rows) is
+    computed and copied out apart when that block has 1024 rows or more."""
+    nb = max(1, min(8, M // 2048))
+    mb = min(M, -(-(-(-M // nb)) // 128) * 128)
+    blocks = -(-M // mb)
+    edges = [i * mb for i in range(blocks)]
+    last = M - edges[-1]
+    if blocks >= 2 and last >= 1024:
+        tail = -(-3 * last // 1024) * 128
+        if tail < last:
+            edges.append(M - tail)
+    return edges
+
+
 # (4200, 2048, 4100): two row blocks and a 33.6 MB B, so the first block runs in K chunks
-# of 640 (the last one 260) as B arrives
+# of 256, 512, 1024 and 2308 as B arrives; the second block (2024 rows) is computed as
+# 1256 + 768 rows
 @pytest.mark.parametrize("shape", [(300, 200, 100), (5000, 700, 300), (9000, 64, 50),
                                    (4200, 2048, 4100)])
 @pytest.mark.parametrize("pinned", [True, False])
@@ -43,8 +61,9 @@ def test_host_entry_against_oracle(shape, pinned, alpha, beta):
     rc = sg.sgemm_f32_host(M, N, K, alpha, bufA, K + 3, bufB, N + 1, beta, bufC, N + 5, stream)
     assert rc == 0
     stream.synchronize()
-    if M * N * K > 10**9:  # oracle on sampled rows of both blocks (block 0 ends at row 2048)
-        rows = np.unique(np.concatenate([np.arange(0, 8), np.arange(2040, 2056),
+    if M * N * K > 10**9:  # oracle on sampled rows: both sides of every block and part edge
+        edges = [r for e in _block_edges(M) for r in range(max(0, e - 4), min(M, e + 4))]
+        rows = np.unique(np.concatenate([np.arange(0, 8), np.array(edges, dtype=np.int64),
                                          np.random.default_rng(M).integers(0, M, 40), [M - 1]]))
         R, S = oracle.sgemm_f64_rows(A, B, C, alpha, beta, rows)
         assert_bound(hC.numpy()[rows], R, S, beta, C.numpy()[rows], f"host {shape} pinned={pinned}")
